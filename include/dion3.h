@@ -1,0 +1,198 @@
+/*
+ * dion3.h -- C ABI of the GB300 (sm_103a) Dion3 / Gram Newton-Schulz library (libdion3.so).
+ *
+ * The library implements the data-parallel hot path of the Dion3 optimizer:
+ *   - a symmetric GEMM (lower triangle computed, upper triangle written as its exact mirror),
+ *   - batched Gram Newton-Schulz orthogonalization with restarts,
+ *   - one Dion3 step (momentum update, exact top-k row selection, orthogonalization of the
+ *     selected rows, W row update, error-feedback decay of the selected rows).
+ *
+ * Citations name a page and a section of it:
+ *   [D3]  "Dion3: Full-Stack Orthogonal Updates", structured summary (paper.rainbus.top):
+ *         prerequisites, "core method" (Theorem 2), "method details" (Algorithms 3 and 4),
+ *         table "structured data" (FLOP formulas), "limitations".
+ *   [D3m] "Dion3: Full-Stack Orthogonal Updates", summary (m.montaan.com).
+ *   [MB]  "Muon: Orthogonalized Momentum and Why It Trains LLMs 2x Cheaper",
+ *         section "Doing an SVD without an SVD".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Matrices are row-major.  A batch of matrices is [batch][rows][cols] with a leading
+ *   dimension `ld` (elements between consecutive rows, >= cols) and a batch stride
+ *   `stride` (elements between consecutive matrices, >= rows*ld when batch > 1).
+ * - All matrix pointers are DEVICE pointers owned by the caller.  `abc`, `restart_after`
+ *   are HOST arrays.  `stream` is a cudaStream_t (NULL = legacy default stream).
+ * - The library allocates no memory, keeps no state between calls and never synchronizes
+ *   the stream.  Scratch memory is the caller's `workspace` (query its size first).
+ * - Host-detectable errors are returned synchronously and nothing is enqueued.  A launch
+ *   failure returns DION3_ECUDA.
+ * - Conditions found on the device are OR-ed into `*status_dev` (a device int, may be
+ *   NULL) as DION3_DEV_* bits; the caller reads it whenever it wants.  No kernel traps.
+ * - Every wait inside a kernel is bounded; a wait that gives up sets DION3_DEV_TIMEOUT
+ *   and the kernel returns (its outputs are then undefined).
+ */
+#ifndef DION3_H
+#define DION3_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DION3_ABI_VERSION 1
+
+/* Return codes. */
+typedef enum {
+  DION3_OK = 0,
+  DION3_EINVAL = 1,        /* a null pointer, negative or inconsistent size, bad schedule */
+  DION3_EUNSUPPORTED = 2,  /* valid but outside what this build supports (dtype mix, limits) */
+  DION3_EWORKSPACE = 3,    /* workspace missing or smaller than the query says */
+  DION3_ECUDA = 4,         /* a CUDA call (launch, tensor-map encode, attribute) failed */
+  DION3_EALIGN = 5         /* a pointer, leading dimension or stride breaks the 16-byte rule */
+} dion3_status;
+
+/* Element types. */
+typedef enum { DION3_BF16 = 0, DION3_FP16 = 1, DION3_FP32 = 2 } dion3_dtype;
+
+/* Bits OR-ed into *status_dev by kernels. */
+#define DION3_DEV_NONFINITE 0x1 /* a non-finite momentum key, norm or input value was seen */
+#define DION3_DEV_TIMEOUT   0x2 /* a bounded wait gave up; outputs of that call are undefined */
+#define DION3_DEV_SELECT    0x4 /* row selection could not certify k rows (internal error) */
+
+/*
+ * dion3_sym_gemm -- D = alpha * A * B^T + beta * C + gamma * I, for results known to be
+ * symmetric.  [D3] prerequisite "symmetric GEMM kernels" (compute the lower triangle and the
+ * diagonal, write the transpose into the upper triangle) and [D3] "technical novelty" (the
+ * fused symmetric alpha*A*B + beta*C the Gram form needs).  [D3m] reports the ~2x over cuBLAS.
+ *
+ *   A : [batch][n][k], element type in_dtype, leading dim lda, batch stride strideA.
+ *   B : same shape and type as A, or NULL for B = A (the Gram product A*A^T).  When B != A
+ *       the caller asserts that A*B^T is symmetric (for Gram Newton-Schulz: products of
+ *       polynomials in the same R, which commute).  Only tiles with row-block >= column-block
+ *       are computed.
+ *   C : [batch][n][n] of out_dtype, read only where beta != 0 and only in its lower triangle
+ *       (diagonal included).  May alias D (same ld and stride).
+ *   D : [batch][n][n] of out_dtype.  Every element is written; D[j][i] is the bit-exact copy
+ *       of D[i][j] for i > j.
+ *   in_dtype  : DION3_BF16 / DION3_FP16 (5th-gen tensor cores, fp32 accumulation) or
+ *               DION3_FP32 (fp32 FFMA, no TF32).
+ *   out_dtype : in_dtype or DION3_FP32 for 16-bit inputs; DION3_FP32 for fp32 inputs.
+ *   Alignment: all pointers 16-byte aligned; ld*elemsize and stride*elemsize multiples of 16.
+ *   k == 0 is allowed (D = beta*C + gamma*I).  n == 0 or batch == 0 is a no-op.
+ *   Errors: EINVAL (nulls, sizes, ld < cols), EALIGN, EUNSUPPORTED (dtype mix), ECUDA.
+ */
+int dion3_sym_gemm(int batch, int n, int k,
+                   const void* A, int64_t lda, int64_t strideA,
+                   const void* B, int64_t ldb, int64_t strideB,
+                   const void* C, int64_t ldc, int64_t strideC,
+                   void* D, int64_t ldd, int64_t strideD,
+                   float alpha, float beta, float gamma,
+                   int in_dtype, int out_dtype,
+                   int* status_dev, void* stream);
+
+/*
+ * dion3_gram_ns_workspace_bytes -- bytes of device workspace dion3_gram_ns needs for these
+ * sizes, dtypes and number of restarts (n_restart).  Returns 0 for invalid sizes.
+ */
+size_t dion3_gram_ns_workspace_bytes(int batch, int n, int m, int x_dtype, int compute_dtype,
+                                     int n_restart);
+
+/*
+ * dion3_gram_ns -- Out = GramNS(X) for a batch of n x m matrices, 1 <= n <= m.
+ * [D3] "core method" Theorem 2 and "method details" Algorithm 3; [MB] for the prescale:
+ *   Xs = X / (||X||_F + eps)  (norm in fp32 on the stored values);
+ *   R = Xs Xs^T;  Q = I;
+ *   for t = 1..T:  Z = a_t I + b_t R + c_t R^2;   Q = Q Z;
+ *                  if t is in restart_after:  Xs = Q Xs;  R = Xs Xs^T;  Q = I;
+ *                  else if t < T:             R = Z R Z;
+ *   Out = Q Xs.
+ * Products with Q = I are skipped (Q = Z), as is the R update a restart or the end makes
+ * dead.  16-bit compute keeps R, Z, Q and the restarted Xs in that type with fp32
+ * accumulation; fp32 compute uses fp32 FFMA throughout.
+ *
+ *   X   : [batch][n][m] of x_dtype (ldx, strideX), not modified.  Any alignment: X is copied
+ *         into the workspace when it cannot be read in place.
+ *   Out : [batch][n][m] of out_dtype (ldo, strideO); 16-byte aligned rows.  Must not
+ *         overlap X or the workspace.
+ *   T, abc : T >= 1 iterations, abc = host float[3*T] = (a_1,b_1,c_1, a_2,b_2,c_2, ...).
+ *   restart_after : host int[n_restart], strictly increasing, each in [1, T-1]; may be NULL
+ *         when n_restart == 0.
+ *   eps : added to the Frobenius norm (the pages use 1e-7).
+ *   compute_dtype : DION3_BF16, DION3_FP16 or DION3_FP32.
+ *   workspace : device buffer of at least dion3_gram_ns_workspace_bytes(...) bytes,
+ *         256-byte aligned.
+ *   Errors: EINVAL (n > m, T < 1, schedule), EWORKSPACE, EALIGN (Out), EUNSUPPORTED, ECUDA.
+ *   Device: DION3_DEV_NONFINITE if a norm is not finite.
+ */
+int dion3_gram_ns(int batch, int n, int m,
+                  const void* X, int64_t ldx, int64_t strideX, int x_dtype,
+                  void* Out, int64_t ldo, int64_t strideO, int out_dtype,
+                  int T, const float* abc, const int* restart_after, int n_restart,
+                  float eps, int compute_dtype,
+                  void* workspace, size_t workspace_bytes,
+                  int* status_dev, void* stream);
+
+/*
+ * dion3_k -- k = ceil(n * f_num / f_den) in exact integers ([D3] "existing work": k = ceil(f n)).
+ * Returns -1 unless n >= 0 and 0 < f_num <= f_den.
+ */
+int dion3_k(int n, int f_num, int f_den);
+
+/*
+ * dion3_step_workspace_bytes -- bytes of workspace dion3_step needs.  0 for invalid sizes.
+ */
+size_t dion3_step_workspace_bytes(int batch, int n, int m, int f_num, int f_den, int norm_p,
+                                  int compute_dtype, int n_restart);
+
+/*
+ * dion3_step -- one Dion3 step on a megabatch of same-shape matrices, n <= m.
+ * [D3] "method details" Algorithm 4, prerequisite "error feedback", prerequisite
+ * "spectral-norm steepest descent" (eta' = eta / sqrt(f)):
+ *   M <- M + G                                  (fp32 state, one rounding)
+ *   key_i = sum_j |M_ij|   (norm_p = 1, the pages' l1 rule)
+ *         = sum_j M_ij^2   (norm_p = 2, same order as the row L2 norm)
+ *   S = the k = ceil(f n) rows with the largest exact keys, ties to the lower row index,
+ *       written ascending to sel_out.  Keys are compared as exact real numbers: fp32 keys
+ *       with a proven error bound decide every row they can, and the rows they cannot are
+ *       re-ranked with exact integer sums on the device.
+ *   O = GramNS(M[S,:])                          (as dion3_gram_ns, compute_dtype)
+ *   W <- (1 - eta' wd) W  (all rows; skipped when wd == 0)
+ *   W[S,:] <- W[S,:] - eta' O,  eta' = eta * sqrt(f_den / f_num)
+ *   M[S,:] <- mu * M[S,:]                       (fp32, one rounding; mu taken as given)
+ *
+ *   W, M : fp32 [batch][n][m], contiguous (ld = m, stride = n*m), updated in place.
+ *   G    : [batch][n][m] contiguous, g_dtype DION3_BF16, DION3_FP16 or DION3_FP32.
+ *   sel_out : int32 [batch][k] device output, ascending row indices.
+ *   Limits: n <= 16384 and m <= 65536 (exact selection); 0 < f_num <= f_den.
+ *   W, M, G, sel_out 16-byte aligned.  Errors as dion3_gram_ns.
+ *   Device: DION3_DEV_NONFINITE (a non-finite momentum or norm), DION3_DEV_SELECT.
+ */
+int dion3_step(int batch, int n, int m,
+               float* W, float* M, const void* G, int g_dtype,
+               int f_num, int f_den, float mu, float eta, float wd, int norm_p,
+               int T, const float* abc, const int* restart_after, int n_restart, float eps,
+               int compute_dtype, int32_t* sel_out,
+               void* workspace, size_t workspace_bytes,
+               int* status_dev, void* stream);
+
+/* Human-readable name of a return code. */
+const char* dion3_status_str(int code);
+
+/* DION3_ABI_VERSION of the loaded library. */
+int dion3_abi_version(void);
+
+/*
+ * dion3_selftest_watchdog -- diagnostic for the bounded-wait machinery (no counterpart on the
+ * pages).  Launches one small kernel that waits on a barrier nothing will ever complete,
+ * giving up after `spin_limit_cycles` clock cycles; it then sets DION3_DEV_TIMEOUT in
+ * *status_dev and returns normally.  status_dev must be non-NULL.
+ */
+int dion3_selftest_watchdog(long long spin_limit_cycles, int* status_dev, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DION3_H */

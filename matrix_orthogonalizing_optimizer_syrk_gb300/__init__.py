@@ -1,0 +1,235 @@
+"""GB300 (sm_103a) Dion3 / Gram Newton-Schulz hot path: Python binding of libdion3.so.
+
+This module only marshals arguments: it turns torch CUDA tensors into device pointers,
+leading dimensions and strides, and calls the C ABI declared in ``include/dion3.h``.
+Every step of the computation runs in the library's CUDA kernels; there is no CPU or
+PyTorch fallback, and a missing library raises at first use.
+
+Entry points (same names as the C ABI, without the prefix):
+
+* ``sym_gemm``  -- D = alpha A B^T + beta C + gamma I for symmetric results, lower
+  triangle computed and mirrored ("Dion3: Full-Stack Orthogonal Updates", prerequisite
+  "symmetric GEMM kernels").
+* ``gram_ns``   -- batched Gram Newton-Schulz with restarts (same page, Theorem 2 and
+  Algorithm 3).
+* ``step``      -- one Dion3 step on a megabatch (same page, Algorithm 4 with error
+  feedback).
+* ``k_of``, ``status_str``, ``workspace_bytes_gram_ns``, ``workspace_bytes_step``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_DIR, "libdion3.so")
+
+BF16, FP16, FP32 = 0, 1, 2
+DEV_NONFINITE, DEV_TIMEOUT, DEV_SELECT = 0x1, 0x2, 0x4
+_DT = {torch.bfloat16: BF16, torch.float16: FP16, torch.float32: FP32}
+
+_c_int, _c_i64, _c_f, _c_p, _c_sz = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+
+# name -> (restype, argtypes); mirrors include/dion3.h
+SIGNATURES = {
+    "dion3_sym_gemm": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_i64, _c_i64, _c_p, _c_i64, _c_i64,
+                                _c_p, _c_i64, _c_i64, _c_p, _c_i64, _c_i64, _c_f, _c_f, _c_f, _c_int, _c_int,
+                                _c_p, _c_p]),
+    "dion3_gram_ns_workspace_bytes": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "dion3_gram_ns": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_i64, _c_i64, _c_int, _c_p, _c_i64, _c_i64, _c_int,
+                               _c_int, ctypes.POINTER(_c_f), ctypes.POINTER(_c_int), _c_int, _c_f, _c_int,
+                               _c_p, _c_sz, _c_p, _c_p]),
+    "dion3_k": (_c_int, [_c_int, _c_int, _c_int]),
+    "dion3_step_workspace_bytes": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "dion3_step": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_f, _c_f, _c_f,
+                            _c_int, _c_int, ctypes.POINTER(_c_f), ctypes.POINTER(_c_int), _c_int, _c_f, _c_int,
+                            _c_p, _c_p, _c_sz, _c_p, _c_p]),
+    "dion3_status_str": (ctypes.c_char_p, [_c_int]),
+    "dion3_abi_version": (_c_int, []),
+    "dion3_selftest_watchdog": (_c_int, [ctypes.c_longlong, _c_p, _c_p]),
+}
+
+_lib = None
+
+
+class Dion3Error(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_str(code)} ({code})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libdion3.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing; build it with "
+                               "`python -m matrix_orthogonalizing_optimizer_syrk_gb300._build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_str(code: int) -> str:
+    return lib().dion3_status_str(int(code)).decode()
+
+
+def k_of(n: int, f_num: int, f_den: int) -> int:
+    return int(lib().dion3_k(int(n), int(f_num), int(f_den)))
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != 0:
+        raise Dion3Error(rc, where)
+
+
+def _dt(t: torch.Tensor) -> int:
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}") from None
+
+
+def _dtype_code(d) -> int:
+    return d if isinstance(d, int) else _DT[d]
+
+
+def _cuda(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    return t
+
+
+def _layout(t: torch.Tensor):
+    """(batch, rows, cols, ld, stride) of a 2-D or 3-D tensor with unit column stride."""
+    if t.dim() == 2:
+        rows, cols = t.shape
+        if t.stride(1) != 1 and cols > 1:
+            raise ValueError("columns must be contiguous")
+        ld = t.stride(0) if rows > 1 else max(cols, 1)
+        return 1, rows, cols, ld, rows * ld
+    if t.dim() == 3:
+        batch, rows, cols = t.shape
+        if t.stride(2) != 1 and cols > 1:
+            raise ValueError("columns must be contiguous")
+        ld = t.stride(1) if rows > 1 else max(cols, 1)
+        return batch, rows, cols, ld, t.stride(0)
+    raise ValueError("expected a 2-D or 3-D tensor")
+
+
+def _stream_ptr(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _abc_arrays(abc, restart_after):
+    trip = [tuple(float(v) for v in t) for t in abc]
+    T = len(trip)
+    flat = (_c_f * (3 * T))(*[v for t in trip for v in t])
+    rs = list(int(r) for r in restart_after)
+    rarr = (_c_int * max(1, len(rs)))(*rs) if rs else (_c_int * 1)(0)
+    return T, flat, rarr, len(rs)
+
+
+def sym_gemm(A: torch.Tensor, C: torch.Tensor | None = None, B: torch.Tensor | None = None, alpha: float = 1.0,
+             beta: float = 0.0, gamma: float = 0.0, out: torch.Tensor | None = None, out_dtype=None,
+             status: torch.Tensor | None = None) -> torch.Tensor:
+    """D = alpha A B^T + beta C + gamma I (B defaults to A); lower triangle computed, upper mirrored."""
+    _cuda(A, "A")
+    batch, n, k, lda, sa = _layout(A)
+    odt = A.dtype if out_dtype is None else out_dtype
+    if out is None:
+        shape = (n, n) if A.dim() == 2 else (batch, n, n)
+        out = torch.empty(shape, dtype=odt, device=A.device)
+    _, _, _, ldd, sd = _layout(_cuda(out, "out"))
+    ldb = sb = 0
+    if B is not None:
+        _, _, _, ldb, sb = _layout(_cuda(B, "B"))
+    ldc = sc = 0
+    if C is not None:
+        _, _, _, ldc, sc = _layout(_cuda(C, "C"))
+    rc = lib().dion3_sym_gemm(batch, n, k, _ptr(A), lda, sa, _ptr(B), ldb, sb, _ptr(C), ldc, sc, _ptr(out), ldd, sd,
+                              float(alpha), float(beta), float(gamma), _dt(A), _dt(out), _ptr(status),
+                              _stream_ptr(A.device))
+    _check(rc, "dion3_sym_gemm")
+    return out
+
+
+def workspace_bytes_gram_ns(batch: int, n: int, m: int, x_dtype, compute, n_restart: int) -> int:
+    return int(lib().dion3_gram_ns_workspace_bytes(batch, n, m, _dtype_code(x_dtype), _dtype_code(compute),
+                                                   n_restart))
+
+
+def gram_ns(X: torch.Tensor, abc, restart_after=(), eps: float = 1e-7, compute=torch.bfloat16,
+            out: torch.Tensor | None = None, out_dtype=None, workspace: torch.Tensor | None = None,
+            status: torch.Tensor | None = None) -> torch.Tensor:
+    """Gram Newton-Schulz of each n x m matrix of X (n <= m)."""
+    _cuda(X, "X")
+    batch, n, m, ldx, sx = _layout(X)
+    odt = (torch.float32 if compute == torch.float32 else X.dtype if X.dtype != torch.float32 else compute) \
+        if out_dtype is None else out_dtype
+    if out is None:
+        out = torch.empty(X.shape, dtype=odt, device=X.device)
+    _, _, _, ldo, so = _layout(_cuda(out, "out"))
+    T, flat, rarr, nr = _abc_arrays(abc, restart_after)
+    need = workspace_bytes_gram_ns(batch, n, m, X.dtype, compute, nr)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=X.device)
+    rc = lib().dion3_gram_ns(batch, n, m, _ptr(X), ldx, sx, _dt(X), _ptr(out), ldo, so, _dt(out), T, flat, rarr, nr,
+                             float(eps), _dtype_code(compute), _ptr(workspace), workspace.numel(), _ptr(status),
+                             _stream_ptr(X.device))
+    _check(rc, "dion3_gram_ns")
+    return out
+
+
+def workspace_bytes_step(batch: int, n: int, m: int, f_num: int, f_den: int, norm_p: int, compute,
+                         n_restart: int) -> int:
+    return int(lib().dion3_step_workspace_bytes(batch, n, m, f_num, f_den, norm_p, _dtype_code(compute), n_restart))
+
+
+def step(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, f=(1, 4), mu: float = 0.95, eta: float = 0.01,
+         wd: float = 0.0, norm_p: int = 1, abc=None, restart_after=(2,), eps: float = 1e-7, compute=torch.bfloat16,
+         sel_out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+         status: torch.Tensor | None = None) -> torch.Tensor:
+    """One Dion3 step on [batch, n, m] (or [n, m]) contiguous W, M (fp32) and G; returns the selected rows."""
+    for t, name in ((W, "W"), (M, "M"), (G, "G")):
+        _cuda(t, name)
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if W.dtype != torch.float32 or M.dtype != torch.float32:
+        raise TypeError("W and M are fp32 state")
+    if W.shape != M.shape or G.shape != M.shape:
+        raise ValueError("W, M, G must have the same shape")
+    batch, n, m, _, _ = _layout(M)
+    f_num, f_den = f
+    k = k_of(n, f_num, f_den)
+    if k < 0:
+        raise ValueError("need 0 < f <= 1")
+    if sel_out is None:
+        shape = (k,) if M.dim() == 2 else (batch, k)
+        sel_out = torch.empty(shape, dtype=torch.int32, device=M.device)
+    T, flat, rarr, nr = _abc_arrays(abc, restart_after)
+    need = workspace_bytes_step(batch, n, m, f_num, f_den, norm_p, compute, nr)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=M.device)
+    rc = lib().dion3_step(batch, n, m, _ptr(W), _ptr(M), _ptr(G), _dt(G), f_num, f_den, float(mu), float(eta),
+                          float(wd), norm_p, T, flat, rarr, nr, float(eps), _dtype_code(compute), _ptr(sel_out),
+                          _ptr(workspace), workspace.numel(), _ptr(status), _stream_ptr(M.device))
+    _check(rc, "dion3_step")
+    return sel_out
+
+
+def selftest_watchdog(spin_limit_cycles: int, status: torch.Tensor) -> None:
+    _cuda(status, "status")
+    rc = lib().dion3_selftest_watchdog(int(spin_limit_cycles), _ptr(status), _stream_ptr(status.device))
+    _check(rc, "dion3_selftest_watchdog")

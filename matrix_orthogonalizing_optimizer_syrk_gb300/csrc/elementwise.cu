@@ -1,0 +1,124 @@
+// Frobenius prescale support ("Muon: Orthogonalized Momentum ...", section "Doing an SVD
+// without an SVD": X / (||X||_F + eps), norm in fp32).
+//
+// The scale itself is never applied in a separate pass: it is folded into the alpha of the
+// first X X^T product (alpha = scale^2) and of the first Q X product (alpha = scale), so the
+// input is read by the GEMMs exactly as stored.  These kernels produce the per-row sums of
+// squares (optionally copying X into the compute dtype on the way) and the per-matrix
+// scale, with a fixed reduction order so that results are deterministic.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace dion3 {
+namespace {
+
+template <typename T>
+__device__ __forceinline__ float to_f(T v);
+template <>
+__device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <>
+__device__ __forceinline__ float to_f<__half>(__half v) { return __half2float(v); }
+
+template <typename T>
+__device__ __forceinline__ T from_f(float v);
+template <>
+__device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+template <>
+__device__ __forceinline__ __half from_f<__half>(float v) { return __float2half_rn(v); }
+
+// One warp per row, grid-stride over all batch*n rows.
+template <typename Tin, typename Tout, bool COPY>
+__global__ void __launch_bounds__(256) rows_sumsq_kernel(int batch, int n, int m, const Tin* X, long long ldx,
+                                                         long long sx, float* rowsq, Tout* Xc, long long ldc,
+                                                         long long sc, int* status) {
+  const long long rows = static_cast<long long>(batch) * n;
+  const int lane = threadIdx.x & 31;
+  const long long w0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long row = w0; row < rows; row += nw) {
+    const long long b = row / n, i = row - b * n;
+    const Tin* src = X + b * sx + i * ldx;
+    Tout* dst = COPY ? Xc + b * sc + i * ldc : nullptr;
+    float acc = 0.f;
+    for (int j = lane; j < m; j += 32) {
+      const float x = to_f<Tin>(src[j]);
+      acc = fmaf(x, x, acc);
+      if (COPY) dst[j] = from_f<Tout>(x);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+      rowsq[row] = acc;
+      if (!isfinite(acc) && status) atomicOr(status, DION3_DEV_NONFINITE);
+    }
+  }
+}
+
+__global__ void finalize_scale_kernel(int batch, int rows, const float* rowsq, float eps, float* scale,
+                                      float* alpha2, int* status) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= batch) return;
+  double s = 0.0;
+  const float* r = rowsq + static_cast<long long>(b) * rows;
+  for (int i = 0; i < rows; ++i) s += static_cast<double>(r[i]);
+  const double sc = 1.0 / (sqrt(s) + static_cast<double>(eps));
+  if (!isfinite(s) && status) atomicOr(status, DION3_DEV_NONFINITE);
+  scale[b] = static_cast<float>(sc);
+  alpha2[b] = static_cast<float>(sc * sc);
+}
+
+template <typename Tin, typename Tout, bool COPY>
+int launch_rows(int batch, int n, int m, const Mat& X, float* rowsq, void* Xc, int64_t ldc, int64_t sc, int* status,
+                cudaStream_t s) {
+  const long long rows = static_cast<long long>(batch) * n;
+  long long blocks = (rows + 7) / 8;
+  const long long cap = static_cast<long long>(sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  rows_sumsq_kernel<Tin, Tout, COPY><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      batch, n, m, static_cast<const Tin*>(X.ptr), X.ld, X.stride, rowsq, static_cast<Tout*>(Xc), ldc, sc, status);
+  return cudaGetLastError() == cudaSuccess ? DION3_OK : DION3_ECUDA;
+}
+
+template <typename Tin>
+int dispatch_out(int batch, int n, int m, const Mat& X, float* rowsq, void* Xc, int64_t ldc, int64_t sc, int cdt,
+                 int* status, cudaStream_t s) {
+  if (!Xc) return launch_rows<Tin, float, false>(batch, n, m, X, rowsq, nullptr, 0, 0, status, s);
+  switch (cdt) {
+    case FP32:
+      return launch_rows<Tin, float, true>(batch, n, m, X, rowsq, Xc, ldc, sc, status, s);
+    case FP16:
+      return launch_rows<Tin, __half, true>(batch, n, m, X, rowsq, Xc, ldc, sc, status, s);
+    default:
+      return launch_rows<Tin, __nv_bfloat16, true>(batch, n, m, X, rowsq, Xc, ldc, sc, status, s);
+  }
+}
+
+}  // namespace
+
+int rows_sumsq_copy(int batch, int n, int m, Mat X, float* rowsq, void* Xc, int64_t ldc, int64_t sc, int cdt,
+                    int* status, cudaStream_t s) {
+  if (batch <= 0 || n <= 0) return DION3_OK;
+  switch (X.dtype) {
+    case FP32:
+      return dispatch_out<float>(batch, n, m, X, rowsq, Xc, ldc, sc, cdt, status, s);
+    case FP16:
+      return dispatch_out<__half>(batch, n, m, X, rowsq, Xc, ldc, sc, cdt, status, s);
+    default:
+      return dispatch_out<__nv_bfloat16>(batch, n, m, X, rowsq, Xc, ldc, sc, cdt, status, s);
+  }
+}
+
+int finalize_scale(int batch, int rows, const float* rowsq, float eps, float* scale, float* alpha2, int* status,
+                   cudaStream_t s) {
+  if (batch <= 0) return DION3_OK;
+  finalize_scale_kernel<<<(batch + 127) / 128, 128, 0, s>>>(batch, rows, rowsq, eps, scale, alpha2, status);
+  return cudaGetLastError() == cudaSuccess ? DION3_OK : DION3_ECUDA;
+}
+
+}  // namespace dion3

@@ -1,0 +1,574 @@
+// 16-bit GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM + TMA) for sm_103a.
+//
+// One persistent kernel template serves the three products Gram Newton-Schulz needs
+// ("Dion3: Full-Stack Orthogonal Updates", method details, Algorithm 3; prerequisite
+// "symmetric GEMM kernels"):
+//   EPI_SYM  D = alpha*A*B^T + beta*C + gamma*I for symmetric results (X X^T, R^2 with the
+//            polynomial epilogue, Q Z, R Z, (R Z) Z).  Only tiles that reach the lower
+//            triangle are computed; the epilogue stores each lower element and its mirror,
+//            so D[j][i] is bit-identical to D[i][j].
+//   EPI_GEN  D = alpha*A*B with B stored K x N (N contiguous, "MN-major"): Q X.
+//   EPI_WUPD like EPI_GEN, but the epilogue adds alpha*acc into W[b][sel[b][r]][:] -- the
+//            Dion3 row update W[S,:] -= eta' O fused into the last product (Algorithm 4).
+//
+// CTA = 192 threads: warp 0 issues TMA loads, warp 1 owns TMEM and issues tcgen05.mma
+// (one thread), warps 2-5 drain the accumulators.  Tiles are BM=128 rows x BN (128 or 256)
+// columns, K in steps of 64 16-bit elements (one 128-byte swizzled row).  Two TMEM
+// accumulators let the epilogue of one tile overlap the main loop of the next.  Every
+// wait is bounded (clock64); a wait that gives up raises DION3_DEV_TIMEOUT and the CTA
+// drains its in-flight copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dion3 {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int NUM_THREADS = 192;
+constexpr long long DEFAULT_SPIN = 4000000000LL;  // clock cycles (about 2 s)
+
+template <int BN>
+struct Cfg {
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int BAR_OFF = STAGES * (A_BYTES + B_BYTES);
+  static constexpr int NBARS = 2 * STAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain
+  static constexpr int SMEM = BAR_OFF + NBARS * 8 + 16 + 1024;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES;
+};
+
+struct KParams {
+  int batch, M, N, K;
+  int tiles_m, tiles_n, tiles_per_batch;
+  long long total_tiles;
+  int num_kb;
+  uint32_t idesc;
+  void* D;
+  long long ldd, sD;
+  int d_type;
+  const void* C;
+  long long ldc, sC;
+  float beta;
+  float alpha;
+  const float* alpha_batch;
+  float gamma;
+  float* W;
+  long long ldw, sW;
+  const int* sel;
+  long long ssel;
+  int w_rows;
+  int* status;
+  long long spin_limit;
+};
+
+// ----------------------------------------------------------------------------- tile order
+template <int EPI, int BN>
+__device__ __forceinline__ void decode_tile(const KParams& p, long long t, int& b, int& mi, int& nj) {
+  b = static_cast<int>(t / p.tiles_per_batch);
+  int r = static_cast<int>(t - static_cast<long long>(b) * p.tiles_per_batch);
+  if constexpr (EPI == EPI_SYM) {
+    // Row block i holds column blocks 0 .. i*BM/BN (the blocks that reach the lower triangle).
+    constexpr int RATIO = BN / BM;
+    int row = 0;
+    for (;;) {
+      const int c = row / RATIO + 1;
+      if (r < c) break;
+      r -= c;
+      ++row;
+    }
+    mi = row;
+    nj = r;
+  } else {
+    mi = r % p.tiles_m;
+    nj = r / p.tiles_m;
+  }
+}
+
+// ----------------------------------------------------------------------------- epilogue
+template <typename T>
+struct Out;
+template <>
+struct Out<float> {
+  static __device__ __forceinline__ float cvt(float v) { return v; }
+  static __device__ __forceinline__ float ld(const float* p) { return *p; }
+};
+template <>
+struct Out<__nv_bfloat16> {
+  static __device__ __forceinline__ __nv_bfloat16 cvt(float v) { return __float2bfloat16_rn(v); }
+  static __device__ __forceinline__ float ld(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+};
+template <>
+struct Out<__half> {
+  static __device__ __forceinline__ __half cvt(float v) { return __float2half_rn(v); }
+  static __device__ __forceinline__ float ld(const __half* p) { return __half2float(*p); }
+};
+
+// 32 consecutive values of one row, written with 16-byte stores (caller checked alignment).
+template <typename T>
+__device__ __forceinline__ void store_row32(T* dst, const T (&o)[32]) {
+  const uint4* src = reinterpret_cast<const uint4*>(o);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < static_cast<int>(32 * sizeof(T) / 16); ++i) d[i] = src[i];
+}
+template <typename T>
+__device__ __forceinline__ void load_row32(const T* src, float (&v)[32]) {
+  T tmp[32];
+  uint4* t = reinterpret_cast<uint4*>(tmp);
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < static_cast<int>(32 * sizeof(T) / 16); ++i) t[i] = s[i];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = Out<T>::ld(&tmp[i]);
+}
+
+__device__ __forceinline__ bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+template <typename T>
+__device__ __forceinline__ void epi_sym(const KParams& p, int b, int r, int c0, float (&acc)[32]) {
+  T* D = static_cast<T*>(p.D) + static_cast<long long>(b) * p.sD;
+  const T* C = static_cast<const T*>(p.C) + static_cast<long long>(b) * p.sC;
+  T* drow = D + static_cast<long long>(r) * p.ldd;
+  const bool interior = (c0 + 31 < p.N) && (c0 + 31 < r);
+  if (p.beta != 0.f) {
+    const T* crow = C + static_cast<long long>(r) * p.ldc;
+    if (interior && aligned16(crow + c0)) {
+      float cv[32];
+      load_row32<T>(crow + c0, cv);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] = fmaf(p.beta, cv[i], acc[i]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int c = c0 + i;
+        if (c < p.N && c <= r) acc[i] = fmaf(p.beta, Out<T>::ld(crow + c), acc[i]);
+      }
+    }
+  }
+  if (p.gamma != 0.f) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (c0 + i == r) acc[i] += p.gamma;
+  }
+  T o[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) o[i] = Out<T>::cvt(acc[i]);
+  if (interior && aligned16(drow + c0)) {
+    store_row32<T>(drow + c0, o);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) D[static_cast<long long>(c0 + i) * p.ldd + r] = o[i];
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int c = c0 + i;
+      if (c < p.N && c <= r) {
+        drow[c] = o[i];
+        if (c < r) D[static_cast<long long>(c) * p.ldd + r] = o[i];
+      }
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void epi_gen(const KParams& p, int b, int r, int c0, float (&acc)[32]) {
+  T* drow = static_cast<T*>(p.D) + static_cast<long long>(b) * p.sD + static_cast<long long>(r) * p.ldd;
+  T o[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) o[i] = Out<T>::cvt(acc[i]);
+  if (c0 + 31 < p.N && aligned16(drow + c0)) {
+    store_row32<T>(drow + c0, o);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (c0 + i < p.N) drow[c0 + i] = o[i];
+  }
+}
+
+__device__ __forceinline__ void epi_wupd(const KParams& p, int b, int r, int c0, const float (&acc)[32]) {
+  const int row = __ldg(p.sel + static_cast<long long>(b) * p.ssel + r);
+  if (row < 0 || row >= p.w_rows) return;  // only after a failed selection
+  float* wrow = p.W + static_cast<long long>(b) * p.sW + static_cast<long long>(row) * p.ldw;
+  if (c0 + 31 < p.N && aligned16(wrow + c0)) {
+    float4* w4 = reinterpret_cast<float4*>(wrow + c0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float4 w = w4[i];
+      w.x += acc[4 * i + 0];
+      w.y += acc[4 * i + 1];
+      w.z += acc[4 * i + 2];
+      w.w += acc[4 * i + 3];
+      w4[i] = w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (c0 + i < p.N) wrow[c0 + i] += acc[i];
+  }
+}
+
+template <int EPI>
+__device__ __forceinline__ void epi_dispatch(const KParams& p, int b, int r, int c0, float (&acc)[32]) {
+  if constexpr (EPI == EPI_WUPD) {
+    epi_wupd(p, b, r, c0, acc);
+  } else {
+    switch (p.d_type) {
+      case FP32:
+        if constexpr (EPI == EPI_SYM) epi_sym<float>(p, b, r, c0, acc); else epi_gen<float>(p, b, r, c0, acc);
+        break;
+      case FP16:
+        if constexpr (EPI == EPI_SYM) epi_sym<__half>(p, b, r, c0, acc); else epi_gen<__half>(p, b, r, c0, acc);
+        break;
+      default:
+        if constexpr (EPI == EPI_SYM) epi_sym<__nv_bfloat16>(p, b, r, c0, acc);
+        else epi_gen<__nv_bfloat16>(p, b, r, c0, acc);
+        break;
+    }
+  }
+}
+
+// Wait that ignores the abort flag (used while draining after an abort), bounded by time.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long limit) {
+  const long long t0 = clock64();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > limit) break;
+  }
+}
+
+// ----------------------------------------------------------------------------- kernel
+template <int BN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const KParams p) {
+  using Cf = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + Cf::STAGES * Cf::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cf::BAR_OFF);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + Cf::NBARS);
+  int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t full0 = ptx::smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * Cf::STAGES;
+  const uint32_t tfull0 = empty0 + 8 * Cf::STAGES;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t drain_bar = tempty0 + 16;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cf::STAGES; ++s) {
+      ptx::mbar_init(full0 + 8 * s, 1);
+      ptx::mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(tfull0 + 8 * a, 1);
+      ptx::mbar_init(tempty0 + 8 * a, 4);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_holder), Cf::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  volatile int* abort = abort_flag;
+  const long long lim = p.spin_limit;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t filled = 0, fill_parity = 0;
+      bool ok = true;
+      for (long long t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
+        int b, mi, nj;
+        decode_tile<EPI, BN>(p, t, b, mi, nj);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!ptx::mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort, lim)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8 * stage;
+          ptx::mbar_arrive_expect_tx(fb, Cf::TX_BYTES);
+          ptx::tma_load_3d(ptx::smem_u32(sA + stage * Cf::A_BYTES), &tmA, fb, kb * BK, mi * BM, b);
+          const uint32_t bdst = ptx::smem_u32(sB + stage * Cf::B_BYTES);
+          if constexpr (!B_MN) {
+            ptx::tma_load_3d(bdst, &tmB, fb, kb * BK, nj * BN, b);
+          } else {
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c)
+              ptx::tma_load_3d(bdst + c * (BK * 128), &tmB, fb, nj * BN + c * 64, kb * BK, b);
+          }
+          filled |= 1u << stage;
+          fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == Cf::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Let every issued copy land before the CTA's shared memory is released.
+        for (int s = 0; s < Cf::STAGES; ++s)
+          if (filled & (1u << s)) drain_wait(full0 + 8 * s, (fill_parity >> s) & 1u, lim);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (long long t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
+        if (!ptx::mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, abort, lim)) break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!ptx::mbar_wait(full0 + 8 * stage, phase, abort, lim)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a_base = ptx::smem_u32(sA + stage * Cf::A_BYTES);
+          const uint32_t b_base = ptx::smem_u32(sB + stage * Cf::B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = ptx::smem_desc_sw128(a_base + kk * 32, 16, 1024);
+            uint64_t bd;
+            if constexpr (!B_MN) bd = ptx::smem_desc_sw128(b_base + kk * 32, 16, 1024);
+            else bd = ptx::smem_desc_sw128(b_base + kk * 16 * 128, BK * 128, 1024);
+            ptx::tc_mma_f16(d_tmem, ad, bd, p.idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::tc_commit(empty0 + 8 * stage);
+          if (++stage == Cf::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::tc_commit(tfull0 + 8 * acc);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // Every MMA this thread issued has completed once the drain barrier fires.
+      ptx::tc_commit(drain_bar);
+      drain_wait(drain_bar, 0, lim);
+    }
+  } else {
+    // ------------------------------------------------ epilogue (warps 2..5)
+    const int ew = warp & 3;  // TMEM lanes 32*ew .. 32*ew+31
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+      int b, mi, nj;
+      decode_tile<EPI, BN>(p, t, b, mi, nj);
+      if (!ptx::mbar_wait(tfull0 + 8 * acc, acc_phase, abort, lim)) break;
+      ptx::tc_fence_after();
+      const float ab = p.alpha * (p.alpha_batch ? __ldg(p.alpha_batch + b) : 1.f);
+      const int r = mi * BM + ew * 32 + lane;
+      const int rmax_warp = mi * BM + ew * 32 + 31;
+      const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        const int c0 = nj * BN + ch * 32;
+        if (c0 >= p.N) break;
+        if (EPI == EPI_SYM && c0 > rmax_warp) break;
+        uint32_t v[32];
+        __syncwarp();
+        if (p.num_kb > 0) {
+          ptx::tmem_ld_32x32b_x32(t_acc + ch * 32, v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        if (r < p.M) {
+          float a[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a[i] = __uint_as_float(v[i]) * ab;
+          epi_dispatch<EPI>(p, b, r, c0, a);
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(tempty0 + 8 * acc);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, Cf::TMEM_COLS);
+  }
+  if (threadIdx.x == 0 && *abort && p.status) atomicOr(p.status, DION3_DEV_TIMEOUT);
+}
+
+__global__ void watchdog_kernel(long long limit, int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bar), 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // Nothing ever arrives on `bar`: the wait must give up on its own.
+    if (!ptx::mbar_wait(ptx::smem_u32(&bar), 0, &abort_flag, limit)) atomicOr(status, DION3_DEV_TIMEOUT);
+  }
+}
+
+// ----------------------------------------------------------------------------- host side
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn get_encode() {
+  static EncodeFn fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeFn>(nullptr);
+    return reinterpret_cast<EncodeFn>(ptr);
+  }();
+  return fn;
+}
+
+// 3-D map over a 16-bit [batch][rows][cols] operand, box = box_cols x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const Mat& m, int rows, int cols, int batch, int box_cols, int box_rows) {
+  EncodeFn enc = get_encode();
+  if (!enc) return false;
+  const cuuint64_t es = 2;
+  cuuint64_t ld_b = static_cast<cuuint64_t>(m.ld) * es;
+  if (ld_b < 16) ld_b = 16;  // K == 0: the map is never read, but must be well formed
+  cuuint64_t st_b = static_cast<cuuint64_t>(m.stride) * es;
+  if (batch <= 1 || st_b == 0) st_b = ld_b * static_cast<cuuint64_t>(rows > 0 ? rows : 1);
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(batch)};
+  cuuint64_t strides[2] = {ld_b, st_b};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt = m.dtype == FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = enc(map, dt, 3, const_cast<void*>(m.ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, bool B_MN, int EPI>
+int launch(const GemmCall& g, cudaStream_t s) {
+  using Cf = Cfg<BN>;
+  KParams p{};
+  p.batch = g.batch;
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.tiles_m = (g.M + BM - 1) / BM;
+  p.tiles_n = (g.N + BN - 1) / BN;
+  if (EPI == EPI_SYM) {
+    int cnt = 0;
+    for (int i = 0; i < p.tiles_m; ++i) cnt += i * BM / BN + 1;
+    p.tiles_per_batch = cnt;
+  } else {
+    p.tiles_per_batch = p.tiles_m * p.tiles_n;
+  }
+  p.total_tiles = static_cast<long long>(p.tiles_per_batch) * g.batch;
+  p.num_kb = (g.K + BK - 1) / BK;
+  p.idesc = ptx::make_idesc_f16(g.A.dtype == FP16 ? 0 : 1, B_MN, BM, BN);
+  p.D = const_cast<void*>(g.D.ptr);
+  p.ldd = g.D.ld;
+  p.sD = g.D.stride;
+  p.d_type = g.D.dtype;
+  p.C = g.C.ptr;
+  p.ldc = g.C.ld;
+  p.sC = g.C.stride;
+  p.beta = g.beta;
+  p.alpha = g.alpha;
+  p.alpha_batch = g.alpha_batch;
+  p.gamma = g.gamma;
+  p.W = g.W;
+  p.ldw = g.ldw;
+  p.sW = g.sW;
+  p.sel = g.sel;
+  p.ssel = g.ssel;
+  p.w_rows = g.w_rows;
+  p.status = g.status;
+  p.spin_limit = g.spin_limit > 0 ? g.spin_limit : DEFAULT_SPIN;
+  if (p.total_tiles == 0) return DION3_OK;
+
+  CUtensorMap ta, tb;
+  // A is [batch][M][K]; with K == 0 the maps still need a non-empty extent.
+  const int kdim = g.K > 0 ? g.K : 1;
+  if (!make_map(&ta, g.A, g.M, kdim, g.batch, BK, BM)) return DION3_ECUDA;
+  if (!B_MN) {
+    if (!make_map(&tb, g.B, g.N, kdim, g.batch, BK, BN)) return DION3_ECUDA;
+  } else {
+    if (!make_map(&tb, g.B, kdim, g.N, g.batch, 64, BK)) return DION3_ECUDA;
+  }
+  auto kern = tc_gemm_kernel<BN, B_MN, EPI>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM) != cudaSuccess)
+    return DION3_ECUDA;
+  long long grid = sm_count();
+  if (grid > p.total_tiles) grid = p.total_tiles;
+  kern<<<static_cast<unsigned>(grid), NUM_THREADS, Cf::SMEM, s>>>(ta, tb, p);
+  return cudaGetLastError() == cudaSuccess ? DION3_OK : DION3_ECUDA;
+}
+
+}  // namespace
+
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 1;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+int gemm_tc(const GemmCall& g, cudaStream_t s) {
+  if (g.batch <= 0 || g.M <= 0 || g.N <= 0) return DION3_OK;
+  switch (g.epi) {
+    case EPI_SYM:
+      return g.M <= 128 ? launch<128, false, EPI_SYM>(g, s) : launch<256, false, EPI_SYM>(g, s);
+    case EPI_GEN:
+      return g.N <= 128 ? launch<128, true, EPI_GEN>(g, s) : launch<256, true, EPI_GEN>(g, s);
+    case EPI_WUPD:
+      return g.N <= 128 ? launch<128, true, EPI_WUPD>(g, s) : launch<256, true, EPI_WUPD>(g, s);
+    default:
+      return DION3_EINVAL;
+  }
+}
+
+int selftest_watchdog(long long spin_limit, int* status, cudaStream_t s) {
+  watchdog_kernel<<<1, 32, 0, s>>>(spin_limit, status);
+  return cudaGetLastError() == cudaSuccess ? DION3_OK : DION3_ECUDA;
+}
+
+}  // namespace dion3

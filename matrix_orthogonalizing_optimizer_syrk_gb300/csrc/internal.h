@@ -1,0 +1,102 @@
+// Internal host interface shared by the translation units of libdion3.so.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "dion3.h"
+
+namespace dion3 {
+
+enum DType { BF16 = DION3_BF16, FP16 = DION3_FP16, FP32 = DION3_FP32 };
+
+inline int dtype_size(int t) { return t == FP32 ? 4 : 2; }
+inline bool dtype_valid(int t) { return t == BF16 || t == FP16 || t == FP32; }
+inline int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// One batched matrix operand: [batch][rows][cols] with leading dim and batch stride (elements).
+struct Mat {
+  const void* ptr = nullptr;
+  int64_t ld = 0;
+  int64_t stride = 0;
+  int dtype = BF16;
+};
+
+enum Epi { EPI_SYM = 0, EPI_GEN = 1, EPI_WUPD = 2 };
+
+// One batched GEMM as the drivers see it.
+//   SYM : D[b] (M x M) = alpha_b * A[b] B[b]^T + beta * C[b] + gamma * I, lower tiles only,
+//         upper triangle mirrored.  A, B are K-major ([b][M][K]).
+//   GEN : D[b] (M x N) = alpha_b * A[b] B[b]; A is [b][M][K], B is [b][K][N] (N contiguous).
+//   WUPD: like GEN, but instead of storing D the epilogue adds alpha_b * acc into
+//         W[b][sel[b][r]][c] (fp32 read-modify-write).
+// alpha_b = alpha * (alpha_batch ? alpha_batch[b] : 1).
+struct GemmCall {
+  int batch = 0, M = 0, N = 0, K = 0;
+  int epi = EPI_SYM;
+  Mat A, B;
+  Mat C;
+  float beta = 0.f;
+  Mat D;
+  float alpha = 1.f;
+  const float* alpha_batch = nullptr;
+  float gamma = 0.f;
+  float* W = nullptr;
+  int64_t ldw = 0, sW = 0;
+  const int* sel = nullptr;
+  int64_t ssel = 0;
+  int w_rows = 0;  // rows of each W matrix (bounds for sel entries)
+  int* status = nullptr;
+  long long spin_limit = 0;  // clock cycles for bounded waits; 0 = default
+};
+
+// 16-bit inputs on the tcgen05 tensor cores (gemm_tc.cu).
+int gemm_tc(const GemmCall& g, cudaStream_t s);
+// fp32 inputs on FFMA (gemm_simt.cu).
+int gemm_simt(const GemmCall& g, cudaStream_t s);
+inline int gemm(const GemmCall& g, cudaStream_t s) {
+  return g.A.dtype == FP32 ? gemm_simt(g, s) : gemm_tc(g, s);
+}
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// ---- elementwise / reduction launchers (elementwise.cu) ----
+// Per-row sum of squares of X (any dtype, any ld) into rowsq[b*n + i] (fp32); optionally
+// copies X into Xc (dtype cdt, ld ldc, stride sc) without scaling.
+int rows_sumsq_copy(int batch, int n, int m, Mat X, float* rowsq, void* Xc, int64_t ldc, int64_t sc,
+                    int cdt, int* status, cudaStream_t s);
+// scale[b] = 1 / (sqrt(sum_i rowsq[b*rows + i]) + eps); alpha2[b] = scale[b]^2.
+int finalize_scale(int batch, int rows, const float* rowsq, float eps, float* scale, float* alpha2,
+                   int* status, cudaStream_t s);
+
+// ---- Dion3 step launchers (step.cu) ----
+struct StepArgs {
+  int batch, n, m, k;
+  float* W;
+  float* M;
+  const void* G;
+  int g_dtype;
+  int norm_p;
+  float mu;
+  float w_decay;  // 1 - eta' * wd (1 means: no decay pass)
+  int32_t* sel;
+  float* key_lo;
+  float* key_hi;
+  uint64_t* exact;  // [batch][n][limbs]
+  void* XS;         // [batch][k][ldx] compute dtype
+  int64_t ldx;
+  int cdt;
+  float* rowsq;  // [batch][k]
+  int* status;
+};
+int step_momentum_keys(const StepArgs& a, cudaStream_t s);
+int step_select(const StepArgs& a, cudaStream_t s);
+int step_gather(const StepArgs& a, cudaStream_t s);
+int step_exact_limbs(int norm_p);
+
+// Watchdog self-test kernel (gemm_tc.cu).
+int selftest_watchdog(long long spin_limit, int* status, cudaStream_t s);
+
+}  // namespace dion3

@@ -1,0 +1,568 @@
+// The memory-bound passes of one Dion3 step ("Dion3: Full-Stack Orthogonal Updates",
+// method details, Algorithm 4, and prerequisite "error feedback"):
+//
+//   pass A  M <- M + G (fp32, one rounding) for every row, optional W <- (1 - eta' wd) W,
+//           and per-row selection keys: fp32 Kahan sums of |M_ij| (or M_ij^2) with a proven
+//           error bound, stored as an interval [lo, hi] that contains the exact key.
+//   pass B  per matrix: the k rows of largest exact key, ties to the lower index, written
+//           ascending.  The intervals decide every row they can; rows whose interval
+//           straddles the boundary are re-ranked with exact integer sums computed on the
+//           device from the stored fp32 row (every fp32 value is an integer multiple of
+//           2^-149, every square one of 2^-298).
+//   pass C  X_S = M[S,:] packed in the compute dtype, per-row sums of squares of X_S for the
+//           Frobenius prescale, and M[S,:] <- mu * M[S,:] (fp32, one rounding).
+// The W row update W[S,:] -= eta' O is fused into the last GEMM's epilogue (gemm_tc.cu).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cfloat>
+
+#include "internal.h"
+
+namespace dion3 {
+namespace {
+
+constexpr int SEL_THREADS = 1024;
+constexpr int MAX_N = 16384;
+
+__device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
+  const float y = __fsub_rn(x, c);
+  const float t = __fadd_rn(s, y);
+  c = __fsub_rn(__fsub_rn(t, s), y);
+  s = t;
+}
+
+template <typename T>
+__device__ __forceinline__ float gval(T v);
+template <>
+__device__ __forceinline__ float gval<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float gval<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <>
+__device__ __forceinline__ float gval<__half>(__half v) { return __half2float(v); }
+
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float (&g)[8]) {
+  if constexpr (sizeof(T) == 2) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const T* h = reinterpret_cast<const T*>(&u);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) g[i] = gval<T>(h[i]);
+  } else {
+    const float4 a = reinterpret_cast<const float4*>(p)[0];
+    const float4 b = reinterpret_cast<const float4*>(p)[1];
+    g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w;
+    g[4] = b.x; g[5] = b.y; g[6] = b.z; g[7] = b.w;
+  }
+}
+
+struct AArgs {
+  long long rows;
+  int m;
+  float* M;
+  const void* G;
+  float* W;
+  float w_decay;
+  bool decay;
+  bool keys;
+  float* key_lo;
+  float* key_hi;
+  int* status;
+};
+
+// ------------------------------------------------------------------------------ pass A
+template <typename TG, int NORM_P, bool VEC>
+__global__ void __launch_bounds__(256) momentum_keys_kernel(const AArgs a) {
+  const int lane = threadIdx.x & 31;
+  const long long w0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  const int m = a.m;
+  for (long long row = w0; row < a.rows; row += nw) {
+    float* Mr = a.M + row * m;
+    const TG* Gr = static_cast<const TG*>(a.G) + row * m;
+    float* Wr = a.W + row * m;
+    float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
+    bool bad = false;
+    if constexpr (VEC) {
+      for (int j = lane * 8; j < m; j += 256) {
+        float g[8];
+        load8<TG>(Gr + j, g);
+        float4* m4 = reinterpret_cast<float4*>(Mr + j);
+        float4 ma = m4[0], mb = m4[1];
+        float x[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+#pragma unroll
+        for (int q = 0; q < 8; ++q) x[q] = __fadd_rn(x[q], g[q]);
+        m4[0] = make_float4(x[0], x[1], x[2], x[3]);
+        m4[1] = make_float4(x[4], x[5], x[6], x[7]);
+        if (a.decay) {
+          float4* w4 = reinterpret_cast<float4*>(Wr + j);
+          float4 wa = w4[0], wb = w4[1];
+          wa.x = __fmul_rn(wa.x, a.w_decay); wa.y = __fmul_rn(wa.y, a.w_decay);
+          wa.z = __fmul_rn(wa.z, a.w_decay); wa.w = __fmul_rn(wa.w, a.w_decay);
+          wb.x = __fmul_rn(wb.x, a.w_decay); wb.y = __fmul_rn(wb.y, a.w_decay);
+          wb.z = __fmul_rn(wb.z, a.w_decay); wb.w = __fmul_rn(wb.w, a.w_decay);
+          w4[0] = wa;
+          w4[1] = wb;
+        }
+        if (a.keys) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            bad |= !isfinite(x[q]);
+            const float t = NORM_P == 1 ? fabsf(x[q]) : __fmul_rn(x[q], x[q]);
+            kahan_add(s[q & 3], c[q & 3], t);
+          }
+        }
+      }
+    } else {
+      for (int j = lane; j < m; j += 32) {
+        const float x = __fadd_rn(Mr[j], gval<TG>(Gr[j]));
+        Mr[j] = x;
+        if (a.decay) Wr[j] = __fmul_rn(Wr[j], a.w_decay);
+        if (a.keys) {
+          bad |= !isfinite(x);
+          const float t = NORM_P == 1 ? fabsf(x) : __fmul_rn(x, x);
+          kahan_add(s[0], c[0], t);
+        }
+      }
+    }
+    if (!a.keys) continue;
+    double tot = static_cast<double>(s[0]) + static_cast<double>(s[1]) + static_cast<double>(s[2]) +
+                 static_cast<double>(s[3]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    const bool any_bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      float lo, hi;
+      if (any_bad) {
+        // Non-finite momentum: flagged; the row ranks as the largest.
+        if (a.status) atomicOr(a.status, DION3_DEV_NONFINITE);
+        lo = hi = __int_as_float(0x7f800000);
+      } else if (!isfinite(tot)) {
+        // fp32 overflow of the running sum: leave the decision to the exact path.
+        lo = 0.f;
+        hi = __int_as_float(0x7f800000);
+      } else {
+        // Kahan sums of nonnegative terms are within (2u + O(N u^2)) of the exact sum; a squared
+        // term adds u more; the fp64 combination of 128 partial sums adds < 2^-45.  2^-21 = 8u
+        // covers all of it with room to spare; the absolute term covers gradual underflow.
+        const double bound = tot * 0x1p-21 + static_cast<double>(m) * 0x1p-146;
+        lo = __double2float_rd(fmax(tot - bound, 0.0));
+        hi = __double2float_ru(tot + bound);
+      }
+      a.key_lo[row] = lo;
+      a.key_hi[row] = hi;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------ pass B helpers
+// Exclusive prefix sum over the block (blockDim.x a multiple of 32); *total gets the sum.
+__device__ int block_exclusive_scan(int v, int* total, int* warp_sums) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int w = lane < nwarps ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const int prefix = (wid > 0 ? warp_sums[wid - 1] : 0) + x - v;
+  *total = warp_sums[nwarps - 1];
+  __syncthreads();
+  return prefix;
+}
+
+// k-th largest (1-based) of n nonnegative-float bit patterns (monotone as unsigned ints).
+__device__ uint32_t radix_kth_largest(const uint32_t* v, int n, int k, uint32_t* hist, int* sh) {
+  uint32_t prefix = 0, mask = 0;
+  int kk = k;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const uint32_t x = v[i];
+      if ((x & mask) == prefix) atomicAdd(&hist[(x >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int cum = 0, d = 255;
+      for (; d > 0; --d) {
+        if (cum + static_cast<int>(hist[d]) >= kk) break;
+        cum += static_cast<int>(hist[d]);
+      }
+      sh[0] = d;
+      sh[1] = kk - cum;
+    }
+    __syncthreads();
+    prefix |= static_cast<uint32_t>(sh[0]) << shift;
+    mask |= 255u << shift;
+    kk = sh[1];
+    __syncthreads();
+  }
+  return prefix;
+}
+
+template <int NL>
+__device__ void limbs_add_shifted(uint64_t (&L)[NL], uint64_t v, int sh) {
+  if (v == 0) return;
+  const int li = sh >> 6, off = sh & 63;
+  const uint64_t lo = v << off;
+  const uint64_t hi = off ? (v >> (64 - off)) : 0ull;
+  uint64_t old = L[li];
+  L[li] += lo;
+  uint64_t add = hi + (L[li] < old ? 1ull : 0ull);
+  for (int q = li + 1; add != 0 && q < NL; ++q) {
+    old = L[q];
+    L[q] += add;
+    add = L[q] < old ? 1ull : 0ull;
+  }
+}
+
+template <int NL>
+__device__ __forceinline__ int limbs_cmp(const uint64_t* a, const uint64_t* b) {
+  for (int q = NL - 1; q >= 0; --q) {
+    if (a[q] != b[q]) return a[q] > b[q] ? 1 : -1;
+  }
+  return 0;
+}
+
+struct BArgs {
+  int n, m, k;
+  const float* M;
+  const float* key_lo;
+  const float* key_hi;
+  uint64_t* exact;
+  int32_t* sel;
+  int* status;
+};
+
+// ------------------------------------------------------------------------------ pass B
+template <int NORM_P>
+__global__ void __launch_bounds__(SEL_THREADS) select_kernel(const BArgs a) {
+  constexpr int NL = NORM_P == 1 ? 5 : 9;
+  constexpr int NB = NORM_P == 1 ? 256 : 512;
+  extern __shared__ __align__(16) uint8_t sm[];
+  __shared__ uint32_t hist[256];
+  __shared__ unsigned long long bkt[NB];
+  __shared__ int warp_sums[32];
+  __shared__ int sh[4];
+  __shared__ int s_bad;
+
+  const int b = blockIdx.x, n = a.n, k = a.k, tid = threadIdx.x, bd = blockDim.x;
+  int32_t* sel = a.sel + static_cast<long long>(b) * k;
+  if (k >= n) {
+    for (int i = tid; i < n; i += bd) sel[i] = i;
+    return;
+  }
+  if (k <= 0) return;
+  uint32_t* lo = reinterpret_cast<uint32_t*>(sm);
+  uint32_t* hi = lo + n;
+  uint16_t* amb = reinterpret_cast<uint16_t*>(hi + n);
+  uint8_t* flag = reinterpret_cast<uint8_t*>(amb + ((n + 1) & ~1));
+  const float* klo = a.key_lo + static_cast<long long>(b) * n;
+  const float* khi = a.key_hi + static_cast<long long>(b) * n;
+  for (int i = tid; i < n; i += bd) {
+    lo[i] = __float_as_uint(klo[i]);
+    hi[i] = __float_as_uint(khi[i]);
+  }
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  // At least k rows have exact key >= L; at most k rows have hi > H.
+  const uint32_t L = radix_kth_largest(lo, n, k, hist, sh);
+  const uint32_t H = radix_kth_largest(hi, n, k + 1, hist, sh);
+  for (int i = tid; i < n; i += bd) flag[i] = lo[i] > H ? 1 : (hi[i] < L ? 0 : 2);
+  __syncthreads();
+
+  const int chunk = (n + bd - 1) / bd;
+  const int i0 = min(n, tid * chunk), i1 = min(n, i0 + chunk);
+  int c_in = 0, c_amb = 0;
+  for (int i = i0; i < i1; ++i) {
+    c_in += flag[i] == 1;
+    c_amb += flag[i] == 2;
+  }
+  int tot_in, tot_amb;
+  block_exclusive_scan(c_in, &tot_in, warp_sums);
+  int pos = block_exclusive_scan(c_amb, &tot_amb, warp_sums);
+  for (int i = i0; i < i1; ++i)
+    if (flag[i] == 2) amb[pos++] = static_cast<uint16_t>(i);
+  __syncthreads();
+
+  int r = k - tot_in;
+  if (r < 0 || r > tot_amb) {
+    if (tid == 0 && a.status) atomicOr(a.status, DION3_DEV_SELECT);
+    r = r < 0 ? 0 : tot_amb;
+  }
+  if (r > 0 && r < tot_amb) {
+    uint64_t* ex = a.exact + static_cast<long long>(b) * n * NL;
+    for (int j = 0; j < tot_amb; ++j) {
+      const int row = amb[j];
+      for (int q = tid; q < NB; q += bd) bkt[q] = 0ull;
+      __syncthreads();
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(a.M + (static_cast<long long>(b) * n + row) * a.m);
+      for (int base = 0; base < a.m; base += bd) {
+        const int e = base + tid;
+        const uint32_t bits = e < a.m ? src[e] : 0u;
+        const uint32_t e8 = (bits >> 23) & 255u;
+        uint32_t mant = (bits & 0x7FFFFFu) | (e8 ? 0x800000u : 0u);
+        if (e8 == 255u) {
+          s_bad = 1;
+          mant = 0;
+        }
+        const uint32_t w = e8 ? e8 - 1u : 0u;
+        const unsigned grp = __match_any_sync(0xffffffffu, w);
+        const bool leader = (threadIdx.x & 31) == (__ffs(grp) - 1);
+        if constexpr (NORM_P == 1) {
+          const unsigned sum = __reduce_add_sync(grp, mant);
+          if (leader && sum) atomicAdd(&bkt[w], static_cast<unsigned long long>(sum));
+        } else {
+          const uint64_t sq = static_cast<uint64_t>(mant) * mant;
+          const unsigned l24 = static_cast<unsigned>(sq & 0xFFFFFFull);
+          const unsigned h24 = static_cast<unsigned>(sq >> 24);
+          const unsigned sl = __reduce_add_sync(grp, l24);
+          const unsigned shh = __reduce_add_sync(grp, h24);
+          if (leader) {
+            if (sl) atomicAdd(&bkt[w], static_cast<unsigned long long>(sl));
+            if (shh) atomicAdd(&bkt[256 + w], static_cast<unsigned long long>(shh));
+          }
+        }
+      }
+      __syncthreads();
+      if (tid == 0) {
+        uint64_t Lm[NL];
+#pragma unroll
+        for (int q = 0; q < NL; ++q) Lm[q] = 0ull;
+        if (s_bad) {
+#pragma unroll
+          for (int q = 0; q < NL; ++q) Lm[q] = ~0ull;
+          if (a.status) atomicOr(a.status, DION3_DEV_NONFINITE);
+        } else {
+          for (int w = 0; w < 256; ++w) {
+            if constexpr (NORM_P == 1) {
+              limbs_add_shifted<NL>(Lm, bkt[w], w);  // value * 2^149 = sum mant * 2^w
+            } else {
+              limbs_add_shifted<NL>(Lm, bkt[w], 2 * w);             // value * 2^298
+              limbs_add_shifted<NL>(Lm, bkt[256 + w], 2 * w + 24);
+            }
+          }
+        }
+        for (int q = 0; q < NL; ++q) ex[static_cast<long long>(j) * NL + q] = Lm[q];
+        s_bad = 0;
+      }
+      __syncthreads();
+    }
+    for (int j = tid; j < tot_amb; j += bd) {
+      const uint64_t* kj = ex + static_cast<long long>(j) * NL;
+      const int ij = amb[j];
+      int rank = 0;
+      for (int q = 0; q < tot_amb; ++q) {
+        if (q == j) continue;
+        const int cmp = limbs_cmp<NL>(ex + static_cast<long long>(q) * NL, kj);
+        if (cmp > 0 || (cmp == 0 && amb[q] < ij)) ++rank;
+      }
+      flag[ij] = rank < r ? 1 : 0;
+    }
+  } else {
+    for (int j = tid; j < tot_amb; j += bd) flag[amb[j]] = (r == tot_amb) ? 1 : 0;
+  }
+  __syncthreads();
+
+  int c_sel = 0;
+  for (int i = i0; i < i1; ++i) c_sel += flag[i] == 1;
+  int tot_sel;
+  int p = block_exclusive_scan(c_sel, &tot_sel, warp_sums);
+  for (int i = i0; i < i1; ++i)
+    if (flag[i] == 1 && p < k) sel[p++] = i;
+  // Never leave an entry unwritten: consumers skip rows outside [0, n).
+  for (int q = tot_sel + tid; q < k; q += bd) sel[q] = -1;
+  if (tid == 0 && tot_sel != k && a.status) atomicOr(a.status, DION3_DEV_SELECT);
+}
+
+// ------------------------------------------------------------------------------ pass C
+struct CArgs {
+  int n, m, k;
+  long long rows;  // batch * k
+  float* M;
+  const int32_t* sel;
+  void* XS;
+  long long ldx;
+  float mu;
+  float* rowsq;
+};
+
+template <typename T>
+__device__ __forceinline__ T cvt_out(float v);
+template <>
+__device__ __forceinline__ float cvt_out<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 cvt_out<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+template <>
+__device__ __forceinline__ __half cvt_out<__half>(float v) { return __float2half_rn(v); }
+
+template <typename TC, bool VEC>
+__global__ void __launch_bounds__(256) gather_kernel(const CArgs a) {
+  const int lane = threadIdx.x & 31;
+  const long long w0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long row = w0; row < a.rows; row += nw) {
+    const long long b = row / a.k;
+    const int i = a.sel[row];
+    TC* dst = static_cast<TC*>(a.XS) + row * a.ldx;
+    if (i < 0 || i >= a.n) {  // only after a failed selection (DION3_DEV_SELECT is set)
+      for (int c = lane; c < a.m; c += 32) dst[c] = cvt_out<TC>(0.f);
+      if (lane == 0) a.rowsq[row] = 0.f;
+      continue;
+    }
+    float* src = a.M + (b * a.n + i) * a.m;
+    float acc = 0.f;
+    if constexpr (VEC) {
+      for (int c = lane * 4; c < a.m; c += 128) {
+        float4* s4 = reinterpret_cast<float4*>(src + c);
+        const float4 x = *s4;
+        acc = fmaf(x.x, x.x, acc);
+        acc = fmaf(x.y, x.y, acc);
+        acc = fmaf(x.z, x.z, acc);
+        acc = fmaf(x.w, x.w, acc);
+        if constexpr (sizeof(TC) == 2) {
+          TC o[4] = {cvt_out<TC>(x.x), cvt_out<TC>(x.y), cvt_out<TC>(x.z), cvt_out<TC>(x.w)};
+          *reinterpret_cast<uint2*>(dst + c) = *reinterpret_cast<const uint2*>(o);
+        } else {
+          *reinterpret_cast<float4*>(dst + c) = x;
+        }
+        *s4 = make_float4(__fmul_rn(a.mu, x.x), __fmul_rn(a.mu, x.y), __fmul_rn(a.mu, x.z), __fmul_rn(a.mu, x.w));
+      }
+    } else {
+      for (int c = lane; c < a.m; c += 32) {
+        const float x = src[c];
+        acc = fmaf(x, x, acc);
+        dst[c] = cvt_out<TC>(x);
+        src[c] = __fmul_rn(a.mu, x);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) a.rowsq[row] = acc;
+  }
+}
+
+template <typename TG, int NORM_P>
+int launch_a(const AArgs& a, bool vec, cudaStream_t s) {
+  long long blocks = (a.rows + 7) / 8;
+  const long long cap = static_cast<long long>(sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  if (vec)
+    momentum_keys_kernel<TG, NORM_P, true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+  else
+    momentum_keys_kernel<TG, NORM_P, false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+  return cudaGetLastError() == cudaSuccess ? DION3_OK : DION3_ECUDA;
+}
+
+template <typename TG>
+int launch_a_p(const AArgs& a, int norm_p, bool vec, cudaStream_t s) {
+  return norm_p == 1 ? launch_a<TG, 1>(a, vec, s) : launch_a<TG, 2>(a, vec, s);
+}
+
+template <typename TC>
+int launch_c(const CArgs& c, bool vec, cudaStream_t s) {
+  long long blocks = (c.rows + 7) / 8;
+  const long long cap = static_cast<long long>(sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) return DION3_OK;
+  if (vec)
+    gather_kernel<TC, true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(c);
+  else
+    gather_kernel<TC, false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(c);
+  return cudaGetLastError() == cudaSuccess ? DION3_OK : DION3_ECUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+int step_exact_limbs(int norm_p) { return norm_p == 1 ? 5 : 9; }
+
+int step_momentum_keys(const StepArgs& s, cudaStream_t st) {
+  AArgs a{};
+  a.rows = static_cast<long long>(s.batch) * s.n;
+  a.m = s.m;
+  a.M = s.M;
+  a.G = s.G;
+  a.W = s.W;
+  a.w_decay = s.w_decay;
+  a.decay = s.w_decay != 1.0f;
+  a.keys = s.k < s.n;
+  a.key_lo = s.key_lo;
+  a.key_hi = s.key_hi;
+  a.status = s.status;
+  if (a.rows == 0) return DION3_OK;
+  const bool vec = (s.m % 8 == 0) && aligned16(s.M) && aligned16(s.G) && aligned16(s.W);
+  switch (s.g_dtype) {
+    case FP32:
+      return launch_a_p<float>(a, s.norm_p, vec, st);
+    case FP16:
+      return launch_a_p<__half>(a, s.norm_p, vec, st);
+    default:
+      return launch_a_p<__nv_bfloat16>(a, s.norm_p, vec, st);
+  }
+}
+
+int step_select(const StepArgs& s, cudaStream_t st) {
+  if (s.batch <= 0 || s.n <= 0) return DION3_OK;
+  if (s.n > MAX_N) return DION3_EUNSUPPORTED;
+  BArgs a{};
+  a.n = s.n;
+  a.m = s.m;
+  a.k = s.k;
+  a.M = s.M;
+  a.key_lo = s.key_lo;
+  a.key_hi = s.key_hi;
+  a.exact = s.exact;
+  a.sel = s.sel;
+  a.status = s.status;
+  const int smem = 11 * s.n + 16;
+  if (s.norm_p == 1) {
+    if (cudaFuncSetAttribute(select_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return DION3_ECUDA;
+    select_kernel<1><<<s.batch, SEL_THREADS, smem, st>>>(a);
+  } else {
+    if (cudaFuncSetAttribute(select_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return DION3_ECUDA;
+    select_kernel<2><<<s.batch, SEL_THREADS, smem, st>>>(a);
+  }
+  return cudaGetLastError() == cudaSuccess ? DION3_OK : DION3_ECUDA;
+}
+
+int step_gather(const StepArgs& s, cudaStream_t st) {
+  CArgs c{};
+  c.n = s.n;
+  c.m = s.m;
+  c.k = s.k;
+  c.rows = static_cast<long long>(s.batch) * s.k;
+  c.M = s.M;
+  c.sel = s.sel;
+  c.XS = s.XS;
+  c.ldx = s.ldx;
+  c.mu = s.mu;
+  c.rowsq = s.rowsq;
+  const bool vec = (s.m % 4 == 0) && aligned16(s.M) && (s.ldx % 8 == 0);
+  switch (s.cdt) {
+    case FP32:
+      return launch_c<float>(c, vec, st);
+    case FP16:
+      return launch_c<__half>(c, vec, st);
+    default:
+      return launch_c<__nv_bfloat16>(c, vec, st);
+  }
+}
+
+}  // namespace dion3

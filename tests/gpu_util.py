@@ -1,0 +1,28 @@
+"""Helpers shared by the GPU parity tests (comparison metrics only; no method arithmetic)."""
+
+import numpy as np
+import torch
+
+
+def rel_frob(got, ref) -> float:
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def to64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def bits32(t) -> np.ndarray:
+    a = t.detach().cpu().numpy() if isinstance(t, torch.Tensor) else np.asarray(t)
+    return a.astype(np.float32, copy=False).view(np.uint32)
+
+
+def exactly_symmetric(t: torch.Tensor) -> bool:
+    a = t.detach().cpu()
+    if a.dtype == torch.bfloat16 or a.dtype == torch.float16:
+        a = a.view(torch.int16)
+    else:
+        a = a.view(torch.int32)
+    return bool(torch.equal(a, a.transpose(-1, -2)))

@@ -1,0 +1,146 @@
+"""Host-only checks of the C ABI: the library loads, exports every symbol the header
+declares, and rejects bad arguments synchronously (before touching the GPU)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import matrix_orthogonalizing_optimizer_syrk_gb300 as d3
+from matrix_orthogonalizing_optimizer_syrk_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dion3.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return d3.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dion3_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = _declared_functions()
+    for required in ["dion3_sym_gemm", "dion3_gram_ns", "dion3_step", "dion3_k", "dion3_status_str",
+                     "dion3_gram_ns_workspace_bytes", "dion3_step_workspace_bytes"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared_functions():
+        assert hasattr(L, name), f"libdion3.so does not export {name}"
+        assert name in d3.SIGNATURES, f"binding does not declare {name}"
+
+
+def test_abi_version(L):
+    assert L.dion3_abi_version() == 1
+
+
+@pytest.mark.parametrize("n,fn,fd,k", [(4096, 1, 4, 1024), (768, 1, 8, 96), (10, 1, 3, 4), (7, 1, 1, 7),
+                                        (0, 1, 4, 0), (5, 0, 1, -1), (5, 2, 1, -1), (5, 1, 0, -1), (-1, 1, 2, -1)])
+def test_k(L, n, fn, fd, k):
+    assert d3.k_of(n, fn, fd) == k
+
+
+def test_status_strings(L):
+    for code in range(6):
+        assert d3.status_str(code).startswith("DION3_")
+
+
+NULL = ctypes.c_void_p(0)
+FAKE = ctypes.c_void_p(0x10000)       # never dereferenced: validation fails first
+FAKE_ODD = ctypes.c_void_p(0x10008)   # 8-byte aligned only
+
+
+def _sym(L, batch=1, n=64, k=64, A=FAKE, lda=64, B=NULL, C=NULL, D=FAKE, ldd=64, beta=0.0, it=0, ot=0):
+    return L.dion3_sym_gemm(batch, n, k, A, lda, n * lda, B, lda, n * lda, C, ldd, n * ldd, D, ldd, n * ldd,
+                            1.0, beta, 0.0, it, ot, NULL, NULL)
+
+
+def test_sym_gemm_validation(L):
+    assert _sym(L, n=-1) == 1
+    assert _sym(L, A=NULL) == 1
+    assert _sym(L, D=NULL) == 1
+    assert _sym(L, beta=1.0) == 1               # C missing
+    assert _sym(L, lda=32) == 1                 # lda < k
+    assert _sym(L, ldd=32) == 1                 # ldd < n
+    assert _sym(L, it=2, ot=0) == 2             # fp32 in, bf16 out
+    assert _sym(L, it=0, ot=1) == 2             # bf16 in, fp16 out
+    assert _sym(L, it=7) == 1
+    assert _sym(L, A=FAKE_ODD) == 5
+    assert _sym(L, lda=68) == 5                 # 136 bytes: not a multiple of 16
+    assert _sym(L, n=0) == 0                    # empty: nothing to do
+    assert _sym(L, batch=0) == 0
+
+
+def _abc(T=5):
+    return (ctypes.c_float * (3 * T))(*([3.4445, -4.7750, 2.0315] * T))
+
+
+def _gram(L, n=64, m=128, X=FAKE, ldx=128, Out=FAKE, ldo=128, T=5, abc=None, rs=(2,), ws=FAKE, wsb=1 << 40,
+          xt=0, ot=0, ct=0, eps=1e-7):
+    abc = _abc(T) if abc is None else abc
+    r = (ctypes.c_int * max(1, len(rs)))(*rs)
+    return L.dion3_gram_ns(1, n, m, X, ldx, n * ldx, xt, Out, ldo, n * ldo, ot, T, abc, r, len(rs), eps, ct,
+                           ws, wsb, NULL, NULL)
+
+
+def test_gram_ns_validation(L):
+    assert _gram(L, n=200, m=100, ldx=100, ldo=104) == 1     # n > m
+    assert _gram(L, T=0) == 1
+    assert _gram(L, rs=(0,)) == 1
+    assert _gram(L, rs=(5,)) == 1
+    assert _gram(L, rs=(3, 2)) == 1
+    assert _gram(L, rs=(2, 2)) == 1
+    assert _gram(L, X=NULL) == 1
+    assert _gram(L, eps=-1.0) == 1
+    assert _gram(L, ws=NULL) == 3
+    assert _gram(L, wsb=16) == 3
+    assert _gram(L, Out=FAKE_ODD) == 5
+    assert _gram(L, X=FAKE_ODD) == 5                         # read in place: must be aligned
+    assert _gram(L, ct=2, ot=0) == 2                         # fp32 compute needs fp32 output
+    nan_abc = (ctypes.c_float * 15)(*([float("nan")] * 15))
+    assert _gram(L, abc=nan_abc) == 1
+
+
+def test_workspace_queries(L):
+    small = d3.workspace_bytes_gram_ns(1, 64, 128, 0, 0, 1)
+    big = d3.workspace_bytes_gram_ns(2, 64, 128, 0, 0, 1)
+    more_r = d3.workspace_bytes_gram_ns(1, 64, 128, 0, 0, 2)
+    copy = d3.workspace_bytes_gram_ns(1, 64, 128, 2, 0, 1)
+    assert 0 < small < big and small < more_r and small < copy
+    assert small % 256 == 0
+    assert d3.workspace_bytes_gram_ns(1, 65, 64, 0, 0, 1) == 0   # n > m
+    s1 = d3.workspace_bytes_step(2, 64, 128, 1, 4, 1, 0, 2)
+    s2 = d3.workspace_bytes_step(2, 64, 128, 1, 2, 1, 0, 2)
+    s3 = d3.workspace_bytes_step(2, 64, 128, 1, 4, 2, 0, 2)
+    assert 0 < s1 < s2 and s1 < s3
+    assert d3.workspace_bytes_step(2, 64, 128, 0, 4, 1, 0, 2) == 0
+
+
+def _step(L, n=64, m=128, W=FAKE, M=FAKE, G=FAKE, sel=FAKE, fn=1, fd=4, p=1, T=5, rs=(2,), ws=FAKE,
+          wsb=1 << 40, mu=0.95):
+    r = (ctypes.c_int * max(1, len(rs)))(*rs)
+    return L.dion3_step(1, n, m, W, M, G, 0, fn, fd, mu, 0.01, 0.0, p, T, _abc(T), r, len(rs), 1e-7, 0, sel, ws,
+                        wsb, NULL, NULL)
+
+
+def test_step_validation(L):
+    assert _step(L, fn=0) == 1
+    assert _step(L, fn=5, fd=4) == 1
+    assert _step(L, p=3) == 1
+    assert _step(L, W=NULL) == 1
+    assert _step(L, sel=NULL) == 1
+    assert _step(L, n=129, m=128) == 1
+    assert _step(L, n=20000, m=20000) == 2
+    assert _step(L, M=FAKE_ODD) == 5
+    assert _step(L, ws=NULL) == 3
+    assert _step(L, mu=float("nan")) == 1
+    assert _step(L, rs=(9,)) == 1

@@ -1,0 +1,102 @@
+"""Gram Newton-Schulz through the C ABI against the float64 oracle.
+
+Tolerances (relative Frobenius): <= 3e-2 with 16-bit compute (R, Z, Q and the restarted X
+are stored in 16 bits, fp32 accumulation); <= 1e-4 in fp32 compute mode.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import matrix_orthogonalizing_optimizer_syrk_gb300 as d3
+import oracle
+import synthetic
+from gpu_util import rel_frob, to64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+JORDAN = (3.4445, -4.7750, 2.0315)
+ABC = [JORDAN] * 5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from matrix_orthogonalizing_optimizer_syrk_gb300 import _build
+
+    _build.build()
+    d3.lib()
+
+
+def test_fp32_mode_256x1024():
+    """fp32 256 x 1024, N(0,1) from seed 0, T = 5 with the Jordan triple, restart after iteration 2."""
+    X = synthetic.gaussian((256, 1024), seed=0, device="cpu").to(DEV)
+    X = X / X.norm()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    O = d3.gram_ns(X, ABC, (2,), compute=torch.float32, status=status)
+    torch.cuda.synchronize()
+    ref = oracle.gram_ns(to64(X), ABC, (2,))
+    assert rel_frob(to64(O), ref) <= 1e-4
+    assert int(status.item()) == 0
+
+
+@pytest.mark.parametrize("n,m", [(1, 8), (17, 40), (96, 2048), (130, 300), (256, 256), (256, 688), (200, 1000)])
+@pytest.mark.parametrize("restarts", [(), (2,), (2, 4)])
+def test_bf16_small(n, m, restarts):
+    X = synthetic.lowrank_plus_noise(n, m, seed=n + m, dtype=torch.bfloat16, device=DEV)
+    O = d3.gram_ns(X, ABC, restarts)
+    torch.cuda.synchronize()
+    assert O.dtype == torch.bfloat16
+    ref = oracle.gram_ns(to64(X), ABC, restarts)
+    assert rel_frob(to64(O), ref) <= 3e-2
+
+
+@pytest.mark.parametrize("compute", [torch.float16, torch.float32])
+def test_other_compute_dtypes(compute):
+    X = synthetic.lowrank_plus_noise(160, 520, seed=5, dtype=torch.float32, device=DEV)
+    O = d3.gram_ns(X, ABC, (2,), compute=compute, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ref = oracle.gram_ns(to64(X), ABC, (2,))
+    assert rel_frob(to64(O), ref) <= (3e-2 if compute != torch.float32 else 1e-4)
+
+
+def test_fp32_input_bf16_compute_copy_path():
+    X = synthetic.gaussian((100, 333), seed=6, device=DEV)       # m % 8 != 0: copied into the workspace
+    O = d3.gram_ns(X, ABC, (2, 4), compute=torch.bfloat16, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert rel_frob(to64(O), oracle.gram_ns(to64(X), ABC, (2, 4))) <= 3e-2
+
+
+def test_batched_strided_per_iteration_coefficients():
+    abc = [(3.4445, -4.7750, 2.0315), (3.0, -3.2, 1.2), (2.5, -2.0, 0.6), (1.875, -1.25, 0.375), (1.5, -0.5, 0.0)]
+    batch, n, m = 6, 120, 512
+    big = synthetic.lowrank_batch(batch, n, m + 64, base_seed=70, dtype=torch.bfloat16, device=DEV)
+    X = big[:, :, :m]
+    O = d3.gram_ns(X, abc, (1, 3))
+    torch.cuda.synchronize()
+    for b in range(batch):
+        assert rel_frob(to64(O[b]), oracle.gram_ns(to64(X[b]), abc, (1, 3))) <= 3e-2
+
+
+def test_output_singular_values_in_band():
+    X = synthetic.lowrank_plus_noise(256, 1024, seed=8, dtype=torch.bfloat16, device=DEV)
+    O = d3.gram_ns(X, ABC, (2,), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    sv = np.linalg.svd(to64(O), compute_uv=False)
+    assert sv.min() > 0.6 and sv.max() < 1.3
+
+
+@pytest.mark.parametrize("shape,count", [((4096, 4096), 128), ((4096, 11008), 96)])
+def test_megabatch_full_size_sampled(shape, count):
+    """7B-shaped megabatches (bf16, restarts after 2 and 4); the oracle checks matrices 0, B/2, B-1."""
+    n, m = shape
+    base = 3000 + (0 if m == n else 1000)
+    X = torch.empty((count, n, m), dtype=torch.bfloat16, device=DEV)
+    for i in range(count):
+        synthetic.lowrank_plus_noise(n, m, base + i, dtype=torch.bfloat16, device=DEV, out=X[i])
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    O = d3.gram_ns(X, ABC, (2, 4), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for i in (0, count // 2, count - 1):
+        ref = oracle.gram_ns(to64(X[i]), ABC, (2, 4))
+        assert rel_frob(to64(O[i]), ref) <= 3e-2

@@ -1,0 +1,146 @@
+"""One Dion3 step through the C ABI against the float64 oracle.
+
+Bars: selected row indices bit-exact; the fp32 momentum M bit-exact (one rounding after
++G, one after *mu); the weight update Delta W within 3e-2 relative Frobenius error of the
+oracle's (16-bit Gram Newton-Schulz); 1e-4 in fp32 compute mode.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import matrix_orthogonalizing_optimizer_syrk_gb300 as d3
+import oracle
+import synthetic
+from gpu_util import bits32, rel_frob, to64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+ABC = [(3.4445, -4.7750, 2.0315)] * 5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from matrix_orthogonalizing_optimizer_syrk_gb300 import _build
+
+    _build.build()
+    d3.lib()
+
+
+def _run_and_check(W, M, G, f, mu, eta, norm_p, restarts, compute=torch.bfloat16, wd=0.0, idx=None, tol=3e-2):
+    """One step on the GPU (whole batch) and on the oracle (matrices in idx); compare."""
+    batch = M.shape[0]
+    idx = range(batch) if idx is None else idx
+    W0 = {i: W[i].cpu().numpy().copy() for i in idx}
+    M0 = {i: M[i].cpu().numpy().copy() for i in idx}
+    Gc = {i: G[i].float().cpu().numpy() for i in idx}
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sel = d3.step(W, M, G, f=f, mu=mu, eta=eta, wd=wd, norm_p=norm_p, abc=ABC, restart_after=restarts,
+                  compute=compute, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for i in idx:
+        W1, M1, S, _ = oracle.dion3_step(W0[i], M0[i], Gc[i], *f, mu=mu, eta=eta, wd=wd, norm_p=norm_p, abc=ABC,
+                                         restart_after=restarts)
+        assert np.array_equal(sel[i].cpu().numpy().astype(np.int64), S), f"matrix {i}: selection differs"
+        assert np.array_equal(bits32(M[i]), bits32(M1)), f"matrix {i}: momentum differs"
+        dW = W[i].double().cpu().numpy() - W0[i]
+        assert rel_frob(dW, W1 - W0[i]) <= tol, f"matrix {i}: weight update off"
+    return sel
+
+
+@pytest.mark.parametrize("n,m", [(64, 256), (130, 1000), (96, 1004)])
+@pytest.mark.parametrize("f", [(1, 4), (1, 8), (3, 5), (1, 1)])
+@pytest.mark.parametrize("norm_p", [1, 2])
+def test_three_steps(n, m, f, norm_p):
+    batch = 3
+    W = synthetic.gaussian((batch, n, m), seed=1, std=0.02, device=DEV)
+    M = torch.zeros((batch, n, m), dtype=torch.float32, device=DEV)
+    for step in range(3):
+        G = synthetic.lowrank_batch(batch, n, m, base_seed=400 + 10 ** 6 * step + n, dtype=torch.bfloat16,
+                                    device=DEV)
+        _run_and_check(W, M, G, f, 0.95, 0.01, norm_p, (2, 4))
+
+
+def test_f1_selects_every_row():
+    n, m = 48, 200
+    W = synthetic.gaussian((2, n, m), seed=2, std=0.02, device=DEV)
+    M = synthetic.gaussian((2, n, m), seed=3, std=0.01, device=DEV)
+    G = synthetic.lowrank_batch(2, n, m, base_seed=50, device=DEV)
+    sel = _run_and_check(W, M, G, (1, 1), 0.9, 0.02, 1, (2,))
+    assert torch.equal(sel.cpu(), torch.arange(n, dtype=torch.int32).expand(2, n))
+
+
+def test_exact_ties_go_to_lower_index():
+    """Duplicated rows have exactly equal keys: the lower row index must win."""
+    n, m = 40, 128
+    base = synthetic.gaussian((5, m), seed=4, std=0.05, dtype=torch.bfloat16, device=DEV)
+    G = base[torch.arange(n, device=DEV) % 5].unsqueeze(0).contiguous()   # rows repeat with period 5
+    M = torch.zeros((1, n, m), device=DEV)
+    W = torch.zeros((1, n, m), device=DEV)
+    for norm_p in (1, 2):
+        _run_and_check(W.clone(), M.clone(), G, (1, 4), 0.95, 0.01, norm_p, (2,))
+
+
+def test_near_ties_resolved_exactly():
+    """Rows that differ from a twin by one fp32 ulp in one entry: the fp32 key intervals overlap
+    and the device must fall back to exact integer sums."""
+    n, m = 64, 512
+    M = synthetic.gaussian((1, n, m), seed=5, std=0.05, device=DEV)
+    src = torch.arange(0, n, 2, device=DEV)
+    M[0, src + 1] = M[0, src]
+    Mi = M.view(torch.int32)
+    Mi[0, src + 1, 7] += torch.where(src % 4 == 0, 1, -1).to(torch.int32)   # +/- one ulp
+    G = torch.zeros((1, n, m), dtype=torch.bfloat16, device=DEV)
+    W = torch.zeros((1, n, m), device=DEV)
+    for norm_p in (1, 2):
+        for f in ((1, 2), (1, 4), (3, 8)):
+            _run_and_check(W.clone(), M.clone(), G, f, 0.95, 0.01, norm_p, (2,))
+
+
+@pytest.mark.parametrize("gdt", [torch.float32, torch.float16])
+def test_gradient_dtypes_and_weight_decay(gdt):
+    n, m = 80, 320
+    W = synthetic.gaussian((2, n, m), seed=6, std=0.02, device=DEV)
+    M = synthetic.gaussian((2, n, m), seed=7, std=0.01, device=DEV)
+    G = synthetic.lowrank_batch(2, n, m, base_seed=60, dtype=gdt, device=DEV)
+    _run_and_check(W, M, G, (1, 4), 0.95, 0.01, 1, (2,), wd=0.1)
+
+
+def test_fp32_compute_mode():
+    n, m = 64, 256
+    W = synthetic.gaussian((2, n, m), seed=8, std=0.02, device=DEV)
+    M = synthetic.gaussian((2, n, m), seed=9, std=0.01, device=DEV)
+    G = synthetic.lowrank_batch(2, n, m, base_seed=80, device=DEV)
+    _run_and_check(W, M, G, (1, 2), 0.95, 0.01, 1, (2,), compute=torch.float32, tol=1e-4)
+
+
+def test_nonfinite_gradient_sets_status():
+    n, m = 32, 64
+    W = torch.zeros((1, n, m), device=DEV)
+    M = torch.zeros((1, n, m), device=DEV)
+    G = synthetic.lowrank_batch(1, n, m, base_seed=90, device=DEV)
+    G[0, 3, 5] = float("nan")
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    d3.step(W, M, G, f=(1, 4), abc=ABC, restart_after=(2,), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & d3.DEV_NONFINITE
+
+
+@pytest.mark.parametrize("shape,count,f", [((768, 2048), 3072, (1, 8)), ((4096, 4096), 128, (1, 4)),
+                                           ((4096, 11008), 96, (1, 4))])
+def test_megabatch_full_size_two_steps(shape, count, f):
+    """Full-size megabatches (MoE experts at f = 1/8, 7B dense shapes at f = 1/4); matrices 0, B/2 and
+    B-1 checked against the oracle over two steps (the second starts from error-feedback state)."""
+    n, m = shape
+    W = torch.empty((count, n, m), dtype=torch.float32, device=DEV)
+    for i in range(count):
+        W[i] = synthetic.gaussian((n, m), seed=5000 + i, std=0.02, device=DEV)
+    M = torch.zeros((count, n, m), dtype=torch.float32, device=DEV)
+    idx = (0, count // 2, count - 1)
+    for step in range(2):
+        G = torch.empty((count, n, m), dtype=torch.bfloat16, device=DEV)
+        for i in range(count):
+            synthetic.lowrank_plus_noise(n, m, 4000 + i + 10 ** 6 * step, dtype=torch.bfloat16, device=DEV, out=G[i])
+        _run_and_check(W, M, G, f, 0.95, 0.01, 1, (2, 4), idx=idx)
+        del G
