@@ -80,7 +80,8 @@ typedef enum { DION3_BF16 = 0, DION3_FP16 = 1, DION3_FP32 = 2 } dion3_dtype;
  *               DION3_FP32 (fp32 FFMA, no TF32).
  *   out_dtype : in_dtype or DION3_FP32 for 16-bit inputs; DION3_FP32 for fp32 inputs.
  *   Alignment: all pointers 16-byte aligned; ld*elemsize and stride*elemsize multiples of 16.
- *   k == 0 is allowed (D = beta*C + gamma*I).  n == 0 or batch == 0 is a no-op.
+ *   k == 0 is allowed (D = beta*C + gamma*I; A and B are then not read and may be NULL).
+ *   n == 0 or batch == 0 is a no-op.
  *   Errors: EINVAL (nulls, sizes, ld < cols), EALIGN, EUNSUPPORTED (dtype mix), ECUDA.
  */
 int dion3_sym_gemm(int batch, int n, int k,
@@ -110,10 +111,16 @@ size_t dion3_gram_ns_workspace_bytes(int batch, int n, int m, int x_dtype, int c
  *   Out = Q Xs.
  * Products with Q = I are skipped (Q = Z), as is the R update a restart or the end makes
  * dead.  16-bit compute keeps R, Z, Q and the restarted Xs in that type with fp32
- * accumulation; fp32 compute uses fp32 FFMA throughout.
+ * accumulation; fp32 compute uses fp32 FFMA throughout.  [D3] Algorithm 3 runs the
+ * iteration in float16 (DION3_FP16): the half-precision rounding of R is what the restarts
+ * repair.  DION3_BF16 iterates work the same way with an 8-bit mantissa, which costs about an
+ * order of magnitude in accuracy.
  *
- *   X   : [batch][n][m] of x_dtype (ldx, strideX), not modified.  Any alignment: X is copied
- *         into the workspace when it cannot be read in place.
+ *   X   : [batch][n][m] of x_dtype (ldx, strideX), not modified.  X is read in place when
+ *         x_dtype == compute_dtype and its pointer, ldx and strideX are 16-byte multiples;
+ *         otherwise it is copied into the workspace.  The workspace query reserves room for
+ *         that copy unless x_dtype == compute_dtype and m * elemsize is a multiple of 16; a
+ *         call that needs the copy without having queried for it returns DION3_EWORKSPACE.
  *   Out : [batch][n][m] of out_dtype (ldo, strideO); 16-byte aligned rows.  Must not
  *         overlap X or the workspace.
  *   T, abc : T >= 1 iterations, abc = host float[3*T] = (a_1,b_1,c_1, a_2,b_2,c_2, ...).
@@ -123,7 +130,8 @@ size_t dion3_gram_ns_workspace_bytes(int batch, int n, int m, int x_dtype, int c
  *   compute_dtype : DION3_BF16, DION3_FP16 or DION3_FP32.
  *   workspace : device buffer of at least dion3_gram_ns_workspace_bytes(...) bytes,
  *         256-byte aligned.
- *   Errors: EINVAL (n > m, T < 1, schedule), EWORKSPACE, EALIGN (Out), EUNSUPPORTED, ECUDA.
+ *   Errors: EINVAL (n > m, T < 1, schedule), EWORKSPACE, EALIGN (Out, workspace),
+ *           EUNSUPPORTED (fp32 compute with a 16-bit output), ECUDA.
  *   Device: DION3_DEV_NONFINITE if a norm is not finite.
  */
 int dion3_gram_ns(int batch, int n, int m,

@@ -113,19 +113,28 @@ def _layout(t: torch.Tensor):
         rows, cols = t.shape
         if t.stride(1) != 1 and cols > 1:
             raise ValueError("columns must be contiguous")
-        ld = t.stride(0) if rows > 1 else max(cols, 1)
+        ld = t.stride(0) if t.stride(0) >= max(cols, 1) else max(cols, 1)
         return 1, rows, cols, ld, rows * ld
     if t.dim() == 3:
         batch, rows, cols = t.shape
         if t.stride(2) != 1 and cols > 1:
             raise ValueError("columns must be contiguous")
-        ld = t.stride(1) if rows > 1 else max(cols, 1)
+        ld = t.stride(1) if t.stride(1) >= max(cols, 1) else max(cols, 1)
         return batch, rows, cols, ld, t.stride(0)
     raise ValueError("expected a 2-D or 3-D tensor")
 
 
 def _stream_ptr(device) -> ctypes.c_void_p:
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _empty_aligned(shape, dtype, device) -> torch.Tensor:
+    """Uninitialised tensor whose rows start on 16-byte boundaries (padded leading dim)."""
+    es = torch.tensor([], dtype=dtype).element_size()
+    q = 16 // es
+    cols = shape[-1]
+    ld = max(q, (cols + q - 1) // q * q)
+    return torch.empty(tuple(shape[:-1]) + (ld,), dtype=dtype, device=device)[..., :cols]
 
 
 def _ptr(t):
@@ -150,7 +159,7 @@ def sym_gemm(A: torch.Tensor, C: torch.Tensor | None = None, B: torch.Tensor | N
     odt = A.dtype if out_dtype is None else out_dtype
     if out is None:
         shape = (n, n) if A.dim() == 2 else (batch, n, n)
-        out = torch.empty(shape, dtype=odt, device=A.device)
+        out = _empty_aligned(shape, odt, A.device)
     _, _, _, ldd, sd = _layout(_cuda(out, "out"))
     ldb = sb = 0
     if B is not None:
@@ -170,16 +179,22 @@ def workspace_bytes_gram_ns(batch: int, n: int, m: int, x_dtype, compute, n_rest
                                                    n_restart))
 
 
-def gram_ns(X: torch.Tensor, abc, restart_after=(), eps: float = 1e-7, compute=torch.bfloat16,
+def gram_ns(X: torch.Tensor, abc, restart_after=(), eps: float = 1e-7, compute=torch.float16,
             out: torch.Tensor | None = None, out_dtype=None, workspace: torch.Tensor | None = None,
             status: torch.Tensor | None = None) -> torch.Tensor:
-    """Gram Newton-Schulz of each n x m matrix of X (n <= m)."""
+    """Gram Newton-Schulz of each n x m matrix of X (n <= m).
+
+    ``compute`` is the storage type of the iterates R, Z, Q and the restarted X (fp32
+    accumulation throughout).  The default is float16, the precision the Dion3 paper runs
+    Gram Newton-Schulz in (method details, Algorithm 3: normalise, then convert to float16);
+    bfloat16 is supported but its 8-bit mantissa costs roughly an order of magnitude in
+    accuracy on the iterates.  The output defaults to X's dtype (fp32 for fp32 compute).
+    """
     _cuda(X, "X")
     batch, n, m, ldx, sx = _layout(X)
-    odt = (torch.float32 if compute == torch.float32 else X.dtype if X.dtype != torch.float32 else compute) \
-        if out_dtype is None else out_dtype
+    odt = (torch.float32 if compute == torch.float32 else X.dtype) if out_dtype is None else out_dtype
     if out is None:
-        out = torch.empty(X.shape, dtype=odt, device=X.device)
+        out = _empty_aligned(tuple(X.shape), odt, X.device)
     _, _, _, ldo, so = _layout(_cuda(out, "out"))
     T, flat, rarr, nr = _abc_arrays(abc, restart_after)
     need = workspace_bytes_gram_ns(batch, n, m, X.dtype, compute, nr)
@@ -198,7 +213,7 @@ def workspace_bytes_step(batch: int, n: int, m: int, f_num: int, f_den: int, nor
 
 
 def step(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, f=(1, 4), mu: float = 0.95, eta: float = 0.01,
-         wd: float = 0.0, norm_p: int = 1, abc=None, restart_after=(2,), eps: float = 1e-7, compute=torch.bfloat16,
+         wd: float = 0.0, norm_p: int = 1, abc=None, restart_after=(2,), eps: float = 1e-7, compute=torch.float16,
          sel_out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
          status: torch.Tensor | None = None) -> torch.Tensor:
     """One Dion3 step on [batch, n, m] (or [n, m]) contiguous W, M (fp32) and G; returns the selected rows."""

@@ -65,7 +65,7 @@ GramLayout gram_layout(int batch, int n, int m, bool need_copy, int cdt, int n_r
 }
 
 struct StepLayout {
-  size_t key_lo, key_hi, exact, rowsq, scale, alpha2, xs;
+  size_t key_lo, key_hi, exact, rowsq, scale, xs;
   CoreLayout core;
   size_t total;
 };
@@ -76,9 +76,8 @@ StepLayout step_layout(int batch, int n, int m, int k, int norm_p, int cdt, int 
   L.key_lo = cv.take(sizeof(float) * static_cast<size_t>(batch) * n);
   L.key_hi = cv.take(sizeof(float) * static_cast<size_t>(batch) * n);
   L.exact = cv.take(sizeof(uint64_t) * static_cast<size_t>(batch) * n * step_exact_limbs(norm_p));
-  L.rowsq = cv.take(sizeof(float) * static_cast<size_t>(batch) * k);
+  L.rowsq = cv.take(sizeof(float) * static_cast<size_t>(batch) * n);
   L.scale = cv.take(sizeof(float) * batch);
-  L.alpha2 = cv.take(sizeof(float) * batch);
   L.xs = cv.take(static_cast<size_t>(batch) * k * round_up(m, 8) * dtype_size(cdt));
   core_layout(cv, L.core, batch, k, m, cdt, n_restart);
   L.total = round_up(static_cast<int64_t>(cv.off), WS_ALIGN);
@@ -185,8 +184,12 @@ int run_core(const Core& c, cudaStream_t s) {
     // Z = c R R + b R + a I
     rc = sym(nn(Rb), nn(Rb), nn(Zb), c.n, cc, nullptr, nn(Rb), b, a);
     if (rc) return rc;
+    size_t Zcur = Zb;
     if (q_identity) {
+      // Q = I Z = Z: Q takes over Z's buffer (still read below as Z); the old Q buffer
+      // becomes the next iteration's Z buffer.
       std::swap(Qb, Zb);
+      Zcur = Qb;
       q_identity = false;
     } else {
       rc = sym(nn(Qb), nn(Zb), nn(Tb), c.n, 1.f, nullptr, none, 0.f, 0.f);
@@ -210,9 +213,9 @@ int run_core(const Core& c, cudaStream_t s) {
       if (rc) return rc;
       q_identity = true;
     } else if (t < c.T) {
-      rc = sym(nn(Rb), nn(Zb), nn(Tb), c.n, 1.f, nullptr, none, 0.f, 0.f);  // R Z
+      rc = sym(nn(Rb), nn(Zcur), nn(Tb), c.n, 1.f, nullptr, none, 0.f, 0.f);  // R Z
       if (rc) return rc;
-      rc = sym(nn(Tb), nn(Zb), nn(Rb), c.n, 1.f, nullptr, none, 0.f, 0.f);  // (R Z) Z
+      rc = sym(nn(Tb), nn(Zcur), nn(Rb), c.n, 1.f, nullptr, none, 0.f, 0.f);  // (R Z) Z
       if (rc) return rc;
     }
   }
@@ -259,8 +262,14 @@ int dion3_sym_gemm(int batch, int n, int k, const void* A, int64_t lda, int64_t 
   if (!dtype_valid(in_dtype) || !dtype_valid(out_dtype)) return DION3_EINVAL;
   if (in_dtype == FP32 ? out_dtype != FP32 : (out_dtype != in_dtype && out_dtype != FP32)) return DION3_EUNSUPPORTED;
   if (batch == 0 || n == 0) return DION3_OK;
-  if (A == nullptr || D == nullptr || (beta != 0.f && C == nullptr)) return DION3_EINVAL;
-  if (lda < (k > 0 ? k : 0) || ldd < n) return DION3_EINVAL;
+  if (D == nullptr || (beta != 0.f && C == nullptr)) return DION3_EINVAL;
+  if (k == 0) {  // A and B are never read: D = beta C + gamma I
+    A = B = D;
+    lda = ldb = ldd;
+    strideA = strideB = strideD;
+  }
+  if (A == nullptr) return DION3_EINVAL;
+  if (lda < k || ldd < n) return DION3_EINVAL;
   if (B == nullptr) {
     B = A;
     ldb = lda;
@@ -273,12 +282,13 @@ int dion3_sym_gemm(int batch, int n, int k, const void* A, int64_t lda, int64_t 
     if (beta != 0.f && strideC < n * ldc) return DION3_EINVAL;
   }
   if (C != nullptr && C == D && beta != 0.f && (ldc != ldd || (batch > 1 && strideC != strideD))) return DION3_EINVAL;
-  if (!al16(A) || !al16(B) || !al16(D) || (beta != 0.f && !al16(C))) return DION3_EALIGN;
-  if (!ld_ok(lda, in_dtype) || !ld_ok(ldb, in_dtype) || !ld_ok(ldd, out_dtype)) return DION3_EALIGN;
-  if (beta != 0.f && !ld_ok(ldc, out_dtype)) return DION3_EALIGN;
+  const bool reads_ab = k > 0;
+  if (!al16(D) || (beta != 0.f && !al16(C))) return DION3_EALIGN;
+  if (reads_ab && (!al16(A) || !al16(B) || !ld_ok(lda, in_dtype) || !ld_ok(ldb, in_dtype))) return DION3_EALIGN;
+  if (!ld_ok(ldd, out_dtype) || (beta != 0.f && !ld_ok(ldc, out_dtype))) return DION3_EALIGN;
   if (batch > 1) {
-    if (!ld_ok(strideA, in_dtype) || !ld_ok(strideB, in_dtype) || !ld_ok(strideD, out_dtype)) return DION3_EALIGN;
-    if (beta != 0.f && !ld_ok(strideC, out_dtype)) return DION3_EALIGN;
+    if (reads_ab && (!ld_ok(strideA, in_dtype) || !ld_ok(strideB, in_dtype))) return DION3_EALIGN;
+    if (!ld_ok(strideD, out_dtype) || (beta != 0.f && !ld_ok(strideC, out_dtype))) return DION3_EALIGN;
   }
   GemmCall g;
   g.batch = batch;
@@ -297,10 +307,16 @@ int dion3_sym_gemm(int batch, int n, int k, const void* A, int64_t lda, int64_t 
   return gemm(g, static_cast<cudaStream_t>(stream));
 }
 
+// The workspace holds a copy of X unless X can be read in place: same dtype as the compute
+// dtype and rows of a whole number of 16-byte units.
+static bool query_needs_copy(int m, int x_dtype, int compute_dtype) {
+  return x_dtype != compute_dtype || (static_cast<int64_t>(m) * dtype_size(x_dtype)) % 16 != 0;
+}
+
 size_t dion3_gram_ns_workspace_bytes(int batch, int n, int m, int x_dtype, int compute_dtype, int n_restart) {
   if (batch < 0 || n < 0 || m < n || n_restart < 0) return 0;
   if (!dtype_valid(x_dtype) || !dtype_valid(compute_dtype)) return 0;
-  return gram_layout(batch, n, m, x_dtype != compute_dtype, compute_dtype, n_restart).total;
+  return gram_layout(batch, n, m, query_needs_copy(m, x_dtype, compute_dtype), compute_dtype, n_restart).total;
 }
 
 int dion3_gram_ns(int batch, int n, int m, const void* X, int64_t ldx, int64_t strideX, int x_dtype, void* Out,
@@ -318,8 +334,8 @@ int dion3_gram_ns(int batch, int n, int m, const void* X, int64_t ldx, int64_t s
   if (ldx < m || ldo < m) return DION3_EINVAL;
   if (batch > 1 && (strideX < n * ldx || strideO < n * ldo)) return DION3_EINVAL;
   if (!al16(Out) || !ld_ok(ldo, out_dtype) || (batch > 1 && !ld_ok(strideO, out_dtype))) return DION3_EALIGN;
-  const bool need_copy = x_dtype != compute_dtype;
-  if (!need_copy && (!al16(X) || !ld_ok(ldx, x_dtype) || (batch > 1 && !ld_ok(strideX, x_dtype)))) return DION3_EALIGN;
+  const bool x_aligned = al16(X) && ld_ok(ldx, x_dtype) && (batch <= 1 || ld_ok(strideX, x_dtype));
+  const bool need_copy = x_dtype != compute_dtype || !x_aligned;
   const GramLayout L = gram_layout(batch, n, m, need_copy, compute_dtype, n_restart);
   if (workspace == nullptr || workspace_bytes < L.total) return DION3_EWORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & (WS_ALIGN - 1)) != 0) return DION3_EALIGN;
@@ -330,19 +346,22 @@ int dion3_gram_ns(int batch, int n, int m, const void* X, int64_t ldx, int64_t s
   float* alpha2 = reinterpret_cast<float*>(ws + L.alpha2);
   const int64_t ldm = round_up(m, 8);
   Mat Xin{X, ldx, strideX, x_dtype};
-  int rc = rows_sumsq_copy(batch, n, m, Xin, rowsq, need_copy ? ws + L.xcopy : nullptr, ldm,
-                           static_cast<int64_t>(n) * ldm, compute_dtype, status_dev, s);
+  int rc = rows_sumsq(batch, n, m, Xin, rowsq, status_dev, s);
   if (rc) return rc;
-  rc = finalize_scale(batch, n, rowsq, eps, scale, alpha2, status_dev, s);
+  rc = finalize_scale(batch, n, rowsq, eps, scale, need_copy ? nullptr : alpha2, status_dev, s);
   if (rc) return rc;
+  if (need_copy) {  // the copy carries the prescale; nothing is folded into the GEMMs
+    rc = scaled_cast(batch, n, m, Xin, scale, ws + L.xcopy, ldm, static_cast<int64_t>(n) * ldm, compute_dtype, s);
+    if (rc) return rc;
+  }
   Core c;
   c.batch = batch;
   c.n = n;
   c.m = m;
   c.cdt = compute_dtype;
   c.X0 = need_copy ? Mat{ws + L.xcopy, ldm, static_cast<int64_t>(n) * ldm, compute_dtype} : Xin;
-  c.xscale = scale;
-  c.alpha2 = alpha2;
+  c.xscale = need_copy ? nullptr : scale;
+  c.alpha2 = need_copy ? nullptr : alpha2;
   c.ws = ws;
   c.L = L.core;
   c.T = T;
@@ -409,6 +428,8 @@ int dion3_step(int batch, int n, int m, float* W, float* M, const void* G, int g
   sa.ldx = ldm;
   sa.cdt = compute_dtype;
   sa.rowsq = reinterpret_cast<float*>(ws + L.rowsq);
+  sa.scale = reinterpret_cast<float*>(ws + L.scale);
+  sa.eps = eps;
   sa.status = status_dev;
   if (wd == 0.f) sa.w_decay = 1.0f;
 
@@ -419,18 +440,12 @@ int dion3_step(int batch, int n, int m, float* W, float* M, const void* G, int g
   if (k == 0) return DION3_OK;
   rc = step_gather(sa, s);
   if (rc) return rc;
-  float* scale = reinterpret_cast<float*>(ws + L.scale);
-  float* alpha2 = reinterpret_cast<float*>(ws + L.alpha2);
-  rc = finalize_scale(batch, k, sa.rowsq, eps, scale, alpha2, status_dev, s);
-  if (rc) return rc;
   Core c;
   c.batch = batch;
   c.n = k;
   c.m = m;
   c.cdt = compute_dtype;
-  c.X0 = Mat{sa.XS, ldm, static_cast<int64_t>(k) * ldm, compute_dtype};
-  c.xscale = scale;
-  c.alpha2 = alpha2;
+  c.X0 = Mat{sa.XS, ldm, static_cast<int64_t>(k) * ldm, compute_dtype};  // already prescaled
   c.ws = ws;
   c.L = L.core;
   c.T = T;

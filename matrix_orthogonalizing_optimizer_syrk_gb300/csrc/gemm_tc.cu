@@ -522,13 +522,21 @@ int launch(const GemmCall& g, cudaStream_t s) {
   if (p.total_tiles == 0) return DION3_OK;
 
   CUtensorMap ta, tb;
-  // A is [batch][M][K]; with K == 0 the maps still need a non-empty extent.
+  // A is [batch][M][K].  With K == 0 nothing is loaded, but the maps must still be well
+  // formed: they then describe a 16-byte-wide window at D, which is never read.
+  Mat Ae = g.A, Be = g.B;
+  if (g.K == 0) {
+    Ae.ptr = Be.ptr = g.D.ptr;
+    Ae.ld = Be.ld = 8;
+    Ae.stride = Be.stride = 8LL * (g.M > g.N ? g.M : g.N);
+    Ae.dtype = Be.dtype = BF16;
+  }
   const int kdim = g.K > 0 ? g.K : 1;
-  if (!make_map(&ta, g.A, g.M, kdim, g.batch, BK, BM)) return DION3_ECUDA;
+  if (!make_map(&ta, Ae, g.M, kdim, g.batch, BK, BM)) return DION3_ECUDA;
   if (!B_MN) {
-    if (!make_map(&tb, g.B, g.N, kdim, g.batch, BK, BN)) return DION3_ECUDA;
+    if (!make_map(&tb, Be, g.N, kdim, g.batch, BK, BN)) return DION3_ECUDA;
   } else {
-    if (!make_map(&tb, g.B, kdim, g.N, g.batch, 64, BK)) return DION3_ECUDA;
+    if (!make_map(&tb, Be, kdim, g.N, g.batch, 64, BK)) return DION3_ECUDA;
   }
   auto kern = tc_gemm_kernel<BN, B_MN, EPI>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM) != cudaSuccess)

@@ -63,13 +63,14 @@ inline int gemm(const GemmCall& g, cudaStream_t s) {
 int sm_count();
 
 // ---- elementwise / reduction launchers (elementwise.cu) ----
-// Per-row sum of squares of X (any dtype, any ld) into rowsq[b*n + i] (fp32); optionally
-// copies X into Xc (dtype cdt, ld ldc, stride sc) without scaling.
-int rows_sumsq_copy(int batch, int n, int m, Mat X, float* rowsq, void* Xc, int64_t ldc, int64_t sc,
-                    int cdt, int* status, cudaStream_t s);
-// scale[b] = 1 / (sqrt(sum_i rowsq[b*rows + i]) + eps); alpha2[b] = scale[b]^2.
+// Per-row sum of squares of X (any dtype, any ld) into rowsq[b*n + i] (fp32).
+int rows_sumsq(int batch, int n, int m, Mat X, float* rowsq, int* status, cudaStream_t s);
+// scale[b] = 1 / (sqrt(sum_i rowsq[b*rows + i]) + eps); alpha2[b] = scale[b]^2 (alpha2 may be null).
 int finalize_scale(int batch, int rows, const float* rowsq, float eps, float* scale, float* alpha2,
                    int* status, cudaStream_t s);
+// Xc[b] = scale[b] * X[b] in the compute dtype cdt (ld ldc, stride sc).
+int scaled_cast(int batch, int n, int m, Mat X, const float* scale, void* Xc, int64_t ldc, int64_t sc, int cdt,
+                cudaStream_t s);
 
 // ---- Dion3 step launchers (step.cu) ----
 struct StepArgs {
@@ -85,10 +86,12 @@ struct StepArgs {
   float* key_lo;
   float* key_hi;
   uint64_t* exact;  // [batch][n][limbs]
-  void* XS;         // [batch][k][ldx] compute dtype
+  void* XS;         // [batch][k][ldx] compute dtype, = scale_b * M[S,:]
   int64_t ldx;
   int cdt;
-  float* rowsq;  // [batch][k]
+  float* rowsq;  // [batch][n]: per-row sum of squares of M after + G
+  float* scale;  // [batch]: 1 / (||M[S,:]||_F + eps)
+  float eps;
   int* status;
 };
 int step_momentum_keys(const StepArgs& a, cudaStream_t s);

@@ -9,8 +9,10 @@
 //           straddles the boundary are re-ranked with exact integer sums computed on the
 //           device from the stored fp32 row (every fp32 value is an integer multiple of
 //           2^-149, every square one of 2^-298).
-//   pass C  X_S = M[S,:] packed in the compute dtype, per-row sums of squares of X_S for the
-//           Frobenius prescale, and M[S,:] <- mu * M[S,:] (fp32, one rounding).
+//           Pass A also stores each row's sum of squares; pass B adds them up over S for the
+//           Frobenius prescale, scale_b = 1 / (||M[S,:]||_F + eps).
+//   pass C  X_S = scale_b * M[S,:] packed in the compute dtype, and M[S,:] <- mu * M[S,:]
+//           (fp32, one rounding).
 // The W row update W[S,:] -= eta' O is fused into the last GEMM's epilogue (gemm_tc.cu).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -67,6 +69,7 @@ struct AArgs {
   bool keys;
   float* key_lo;
   float* key_hi;
+  float* rowsq;
   int* status;
 };
 
@@ -82,6 +85,7 @@ __global__ void __launch_bounds__(256) momentum_keys_kernel(const AArgs a) {
     const TG* Gr = static_cast<const TG*>(a.G) + row * m;
     float* Wr = a.W + row * m;
     float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
+    float q2[4] = {0.f, 0.f, 0.f, 0.f};  // sums of squares for the Frobenius prescale
     bool bad = false;
     if constexpr (VEC) {
       for (int j = lane * 8; j < m; j += 256) {
@@ -104,6 +108,8 @@ __global__ void __launch_bounds__(256) momentum_keys_kernel(const AArgs a) {
           w4[0] = wa;
           w4[1] = wb;
         }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) q2[q & 3] = fmaf(x[q], x[q], q2[q & 3]);
         if (a.keys) {
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
@@ -117,6 +123,7 @@ __global__ void __launch_bounds__(256) momentum_keys_kernel(const AArgs a) {
       for (int j = lane; j < m; j += 32) {
         const float x = __fadd_rn(Mr[j], gval<TG>(Gr[j]));
         Mr[j] = x;
+        q2[0] = fmaf(x, x, q2[0]);
         if (a.decay) Wr[j] = __fmul_rn(Wr[j], a.w_decay);
         if (a.keys) {
           bad |= !isfinite(x);
@@ -125,6 +132,11 @@ __global__ void __launch_bounds__(256) momentum_keys_kernel(const AArgs a) {
         }
       }
     }
+    double sq = static_cast<double>(q2[0]) + static_cast<double>(q2[1]) + static_cast<double>(q2[2]) +
+                static_cast<double>(q2[3]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    if (lane == 0) a.rowsq[row] = static_cast<float>(sq);
     if (!a.keys) continue;
     double tot = static_cast<double>(s[0]) + static_cast<double>(s[1]) + static_cast<double>(s[2]) +
                  static_cast<double>(s[3]);
@@ -244,8 +256,30 @@ struct BArgs {
   const float* key_hi;
   uint64_t* exact;
   int32_t* sel;
+  const float* rowsq;
+  float* scale;
+  float eps;
   int* status;
 };
+
+// scale[b] = 1 / (sqrt(sum of rowsq over the selected rows) + eps), summed in a fixed order by
+// warp 0 (lane l takes entries l, l+32, ...; then a fixed shuffle tree).
+__device__ void selected_scale(const BArgs& a, int b, const int32_t* sel) {
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  const float* rq = a.rowsq + static_cast<long long>(b) * a.n;
+  double acc = 0.0;
+  for (int j = lane; j < a.k; j += 32) {
+    const int i = sel[j];
+    if (i >= 0 && i < a.n) acc += static_cast<double>(rq[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) {
+    if (!isfinite(acc) && a.status) atomicOr(a.status, DION3_DEV_NONFINITE);
+    a.scale[b] = static_cast<float>(1.0 / (sqrt(acc) + static_cast<double>(a.eps)));
+  }
+}
 
 // ------------------------------------------------------------------------------ pass B
 template <int NORM_P>
@@ -263,6 +297,8 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const BArgs a) {
   int32_t* sel = a.sel + static_cast<long long>(b) * k;
   if (k >= n) {
     for (int i = tid; i < n; i += bd) sel[i] = i;
+    __syncthreads();
+    selected_scale(a, b, sel);
     return;
   }
   if (k <= 0) return;
@@ -386,6 +422,8 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const BArgs a) {
   // Never leave an entry unwritten: consumers skip rows outside [0, n).
   for (int q = tot_sel + tid; q < k; q += bd) sel[q] = -1;
   if (tid == 0 && tot_sel != k && a.status) atomicOr(a.status, DION3_DEV_SELECT);
+  __syncthreads();
+  selected_scale(a, b, sel);
 }
 
 // ------------------------------------------------------------------------------ pass C
@@ -397,7 +435,7 @@ struct CArgs {
   void* XS;
   long long ldx;
   float mu;
-  float* rowsq;
+  const float* scale;
 };
 
 template <typename T>
@@ -420,38 +458,29 @@ __global__ void __launch_bounds__(256) gather_kernel(const CArgs a) {
     TC* dst = static_cast<TC*>(a.XS) + row * a.ldx;
     if (i < 0 || i >= a.n) {  // only after a failed selection (DION3_DEV_SELECT is set)
       for (int c = lane; c < a.m; c += 32) dst[c] = cvt_out<TC>(0.f);
-      if (lane == 0) a.rowsq[row] = 0.f;
       continue;
     }
     float* src = a.M + (b * a.n + i) * a.m;
-    float acc = 0.f;
+    const float f = a.scale[b];
     if constexpr (VEC) {
       for (int c = lane * 4; c < a.m; c += 128) {
         float4* s4 = reinterpret_cast<float4*>(src + c);
         const float4 x = *s4;
-        acc = fmaf(x.x, x.x, acc);
-        acc = fmaf(x.y, x.y, acc);
-        acc = fmaf(x.z, x.z, acc);
-        acc = fmaf(x.w, x.w, acc);
         if constexpr (sizeof(TC) == 2) {
-          TC o[4] = {cvt_out<TC>(x.x), cvt_out<TC>(x.y), cvt_out<TC>(x.z), cvt_out<TC>(x.w)};
+          TC o[4] = {cvt_out<TC>(x.x * f), cvt_out<TC>(x.y * f), cvt_out<TC>(x.z * f), cvt_out<TC>(x.w * f)};
           *reinterpret_cast<uint2*>(dst + c) = *reinterpret_cast<const uint2*>(o);
         } else {
-          *reinterpret_cast<float4*>(dst + c) = x;
+          *reinterpret_cast<float4*>(dst + c) = make_float4(x.x * f, x.y * f, x.z * f, x.w * f);
         }
         *s4 = make_float4(__fmul_rn(a.mu, x.x), __fmul_rn(a.mu, x.y), __fmul_rn(a.mu, x.z), __fmul_rn(a.mu, x.w));
       }
     } else {
       for (int c = lane; c < a.m; c += 32) {
         const float x = src[c];
-        acc = fmaf(x, x, acc);
-        dst[c] = cvt_out<TC>(x);
+        dst[c] = cvt_out<TC>(x * f);
         src[c] = __fmul_rn(a.mu, x);
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) a.rowsq[row] = acc;
   }
 }
 
@@ -503,6 +532,7 @@ int step_momentum_keys(const StepArgs& s, cudaStream_t st) {
   a.keys = s.k < s.n;
   a.key_lo = s.key_lo;
   a.key_hi = s.key_hi;
+  a.rowsq = s.rowsq;
   a.status = s.status;
   if (a.rows == 0) return DION3_OK;
   const bool vec = (s.m % 8 == 0) && aligned16(s.M) && aligned16(s.G) && aligned16(s.W);
@@ -528,6 +558,9 @@ int step_select(const StepArgs& s, cudaStream_t st) {
   a.key_hi = s.key_hi;
   a.exact = s.exact;
   a.sel = s.sel;
+  a.rowsq = s.rowsq;
+  a.scale = s.scale;
+  a.eps = s.eps;
   a.status = s.status;
   const int smem = 11 * s.n + 16;
   if (s.norm_p == 1) {
@@ -553,7 +586,7 @@ int step_gather(const StepArgs& s, cudaStream_t st) {
   c.XS = s.XS;
   c.ldx = s.ldx;
   c.mu = s.mu;
-  c.rowsq = s.rowsq;
+  c.scale = s.scale;
   const bool vec = (s.m % 4 == 0) && aligned16(s.M) && (s.ldx % 8 == 0);
   switch (s.cdt) {
     case FP32:

@@ -26,3 +26,16 @@ def exactly_symmetric(t: torch.Tensor) -> bool:
     else:
         a = a.view(torch.int32)
     return bool(torch.equal(a, a.transpose(-1, -2)))
+
+
+def aligned_copy(t: torch.Tensor) -> torch.Tensor:
+    """Same values, leading dimension rounded up so that each row starts on 16 bytes
+    (the documented layout rule of the symmetric GEMM's inputs)."""
+    es = t.element_size()
+    q = 16 // es
+    cols = t.shape[-1]
+    ld = max(q, (cols + q - 1) // q * q)
+    buf = torch.zeros(t.shape[:-1] + (ld,), dtype=t.dtype, device=t.device)
+    view = buf[..., :cols]
+    view.copy_(t)
+    return view

@@ -104,7 +104,10 @@ def test_gram_ns_validation(L):
     assert _gram(L, ws=NULL) == 3
     assert _gram(L, wsb=16) == 3
     assert _gram(L, Out=FAKE_ODD) == 5
-    assert _gram(L, X=FAKE_ODD) == 5                         # read in place: must be aligned
+    # a misaligned X of the compute dtype needs the copy buffer the query did not reserve
+    no_copy = d3.workspace_bytes_gram_ns(1, 64, 128, 0, 0, 1)
+    assert _gram(L, X=FAKE_ODD, wsb=no_copy) == 3
+    assert _gram(L, ldx=132, wsb=no_copy) == 3              # 264-byte rows: copied, too
     assert _gram(L, ct=2, ot=0) == 2                         # fp32 compute needs fp32 output
     nan_abc = (ctypes.c_float * 15)(*([float("nan")] * 15))
     assert _gram(L, abc=nan_abc) == 1

@@ -12,7 +12,7 @@ import torch
 import matrix_orthogonalizing_optimizer_syrk_gb300 as d3
 import oracle
 import synthetic
-from gpu_util import exactly_symmetric, rel_frob, to64
+from gpu_util import aligned_copy, exactly_symmetric, rel_frob, to64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -31,7 +31,7 @@ def _lib():
 @pytest.mark.parametrize("k", [1, 64, 100, 1000])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
 def test_syrk_small(n, k, dtype):
-    A = synthetic.gaussian((n, k), seed=n * 7 + k, std=k ** -0.5, dtype=dtype, device=DEV)
+    A = aligned_copy(synthetic.gaussian((n, k), seed=n * 7 + k, std=k ** -0.5, dtype=dtype, device=DEV))
     D = d3.sym_gemm(A)
     torch.cuda.synchronize()
     assert exactly_symmetric(D)
@@ -44,7 +44,7 @@ def test_syrk_small(n, k, dtype):
 @pytest.mark.parametrize("alpha,beta,gamma", [(1.0, 1.0, 0.0), (2.0315, -4.775, 3.4445), (0.5, 0.0, 1.0)])
 def test_epilogue_beta_gamma(n, k, dtype, alpha, beta, gamma):
     A = synthetic.gaussian((n, k), seed=11, std=k ** -0.5, dtype=dtype, device=DEV)
-    C = synthetic.symmetric_gaussian(n, seed=12, dtype=dtype, device=DEV)
+    C = aligned_copy(synthetic.symmetric_gaussian(n, seed=12, dtype=dtype, device=DEV))
     D = d3.sym_gemm(A, C=C, alpha=alpha, beta=beta, gamma=gamma)
     torch.cuda.synchronize()
     assert exactly_symmetric(D)
@@ -55,7 +55,7 @@ def test_epilogue_beta_gamma(n, k, dtype, alpha, beta, gamma):
 def test_in_place_c_equals_d():
     n, k = 384, 256
     A = synthetic.gaussian((n, k), seed=13, std=k ** -0.5, dtype=torch.bfloat16, device=DEV)
-    C = synthetic.symmetric_gaussian(n, seed=14, dtype=torch.bfloat16, device=DEV)
+    C = aligned_copy(synthetic.symmetric_gaussian(n, seed=14, dtype=torch.bfloat16, device=DEV))
     ref = oracle.sym_gemm(to64(A), to64(C), 1.0, 1.0, 0.5)
     d3.sym_gemm(A, C=C, beta=1.0, gamma=0.5, out=C)
     torch.cuda.synchronize()
@@ -93,8 +93,8 @@ def test_batched_strided_and_fp32_out(dtype):
 def test_k_zero():
     n = 130
     A = torch.empty((n, 0), dtype=torch.bfloat16, device=DEV)
-    C = synthetic.symmetric_gaussian(n, seed=17, dtype=torch.bfloat16, device=DEV)
-    D = d3.sym_gemm(A, C=C, beta=2.0, gamma=1.0)
+    C = aligned_copy(synthetic.symmetric_gaussian(n, seed=17, dtype=torch.bfloat16, device=DEV))
+    D = d3.sym_gemm(A, C=C, beta=2.0, gamma=1.0, out=aligned_copy(torch.empty_like(C)))
     torch.cuda.synchronize()
     assert exactly_symmetric(D)
     ref = 2.0 * to64(C) + np.eye(n)
