@@ -1,0 +1,527 @@
+#!/usr/bin/env python3
+"""Benchmark of the Dion3 / Gram Newton-Schulz hot path on GB300 (one process per GPU).
+
+Headline step (the whole hot path): one Dion3 step over the two megabatches of a 7B dense
+model's hidden matrices -- 128 x (4096 x 4096) and 96 x (4096 x 11008) -- with f = 1/4
+(k = 1024 rows), mu = 0.95, eta = 0.01 (eta' = 0.02), l1 row selection, T = 5 with the
+Jordan triple (3.4445, -4.7750, 2.0315), restarts after iterations 2 and 4, Gram iterates in
+float16.  State: W fp32 N(0, 0.02), M fp32 starting at zero, G bf16 low-rank-plus-noise
+(seed 4000 + matrix index + 10^6 * set), two pre-generated G sets alternating step by step.
+All inputs are resident in HBM (65 GB per step, far larger than the 129 MB L2).
+
+The JSON line also carries:
+  phases       device time per phase (CUDA events recorded by the library on its stream),
+  roofline     for the dominant phase's kernel,
+  e2e          the same step fed from pinned HOST memory (G copied in, selected rows copied
+               out, every step),
+  gram_ns      Gram Newton-Schulz matrices/s on the 7B megabatches (bf16, f = 1, restarts 2,4),
+  sym_gemm     the symmetric-GEMM sweep (TFLOP/s on n^2 k useful FLOPs, vs torch.matmul),
+  cpu_baseline the float64 oracle on a bounded sample of the same step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Gram-NS matrices/s & Dion3 step ms per megabatch; sym-GEMM TFLOP/s vs bf16 peak"
+JORDAN = (3.4445, -4.7750, 2.0315)
+T_ITERS = 5
+ABC = [JORDAN] * T_ITERS
+RESTARTS = (2, 4)
+MEGABATCHES = [(128, 4096, 4096), (96, 4096, 11008)]  # (batch, n, m): attention and MLP shapes
+F = (1, 4)
+MU, ETA = 0.95, 0.01
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+WORKLOAD = ("dion3_step f=1/4 on 7B dense shapes: megabatches 128x4096x4096 + 96x4096x11008 "
+            "(k=1024, alpha'=4 and 10.75), T=5 Jordan triple, restarts after 2 and 4, mu=0.95, eta=0.01, l1 "
+            "selection, fp16 Gram iterates, W/M fp32, G bf16")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-sub", action="store_true", help="skip the Gram-NS and sym-GEMM sub-measurements")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+def gram_flops(k: int, m: int, T: int = T_ITERS, restarts=RESTARTS) -> int:
+    """(4T + 3a - 3) k^3 + r * 3 (a - 1) k^3 with a = m / k, in exact integers (useful FLOPs)."""
+    r = len(restarts)
+    return (4 * T - 3) * k ** 3 + 3 * m * k * k + r * 3 * (m * k * k - k ** 3)
+
+
+def k_rows(n: int) -> int:
+    return -((-n * F[0]) // F[1])
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.proc = None
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(index), "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError as e:
+            self.err = str(e)
+
+    def stop(self):
+        if self.proc is None:
+            return {"error": getattr(self, "err", "nvidia-smi unavailable")}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(self.NAMES, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"error": "no samples"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- inputs
+def step_inputs(torch, synthetic, dev, rank: int):
+    mbs = []
+    idx0 = 0
+    for (B, n, m) in MEGABATCHES:
+        W = torch.empty((B, n, m), dtype=torch.float32, device=dev)
+        for i in range(B):
+            W[i].copy_(synthetic.gaussian((n, m), seed=5000 + idx0 + i + 10 ** 5 * rank, std=0.02, device=dev))
+        M = torch.zeros((B, n, m), dtype=torch.float32, device=dev)
+        Gs = []
+        for s in range(2):
+            G = torch.empty((B, n, m), dtype=torch.bfloat16, device=dev)
+            for i in range(B):
+                synthetic.lowrank_plus_noise(n, m, 4000 + idx0 + i + 10 ** 6 * s + 10 ** 5 * rank,
+                                             dtype=torch.bfloat16, device=dev, out=G[i])
+            Gs.append(G)
+        sel = torch.empty((B, k_rows(n)), dtype=torch.int32, device=dev)
+        mbs.append({"B": B, "n": n, "m": m, "W": W, "M": M, "Gs": Gs, "sel": sel})
+        idx0 += B
+    return mbs
+
+
+# ----------------------------------------------------------------------------- ours
+def run_ours(args):
+    import torch
+
+    import matrix_orthogonalizing_optimizer_syrk_gb300 as d3
+    import synthetic
+    from matrix_orthogonalizing_optimizer_syrk_gb300 import _build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    d3.lib()
+    peaks, peaks_kind = load_peaks()
+
+    mbs = step_inputs(torch, synthetic, dev, rank)
+    ws_bytes = max(d3.workspace_bytes_step(x["B"], x["n"], x["m"], F[0], F[1], 1, torch.float16, len(RESTARTS))
+                   for x in mbs)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def one_step(s_idx, events=None):
+        for gi, x in enumerate(mbs):
+            d3.step(x["W"], x["M"], x["Gs"][s_idx % 2], f=F, mu=MU, eta=ETA, norm_p=1, abc=ABC,
+                    restart_after=RESTARTS, compute=torch.float16, sel_out=x["sel"], workspace=ws, status=status,
+                    events=None if events is None else events[gi])
+
+    for s in range(args.warmup):
+        one_step(s)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    phase_ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in mbs] for _ in range(K)]
+    for step_evs in phase_ev:
+        for evs in step_evs:
+            for e in evs:
+                e.record()  # creates the event handle the library records into
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    t0.record()
+    for s in range(K):
+        one_step(args.warmup + s, phase_ev[s])
+    t1.record()
+    torch.cuda.synchronize()
+    wall1 = time.perf_counter()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    ms_rank = ms_total / K
+    if dist is not None:
+        tt = torch.tensor([ms_rank], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_rank = float(tt.item())
+    dev_status = int(status.item())
+
+    # phase split (sum over steps, per megabatch)
+    names = ["momentum_keys", "select", "gather", "gram_ns_products"]
+    per_mb = []
+    for gi, x in enumerate(mbs):
+        acc = [0.0] * 4
+        for s in range(K):
+            evs = phase_ev[s][gi]
+            for p in range(4):
+                acc[p] += evs[p].elapsed_time(evs[p + 1])
+        per_mb.append([a / K for a in acc])  # ms per step
+    hbm = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
+    tc_sus = float(peaks.get("bf16_tflops_sustained", PEAKS_FALLBACK["bf16_tflops_sustained"]))
+    bytesA = sum(10.0 * x["B"] * x["n"] * x["m"] for x in mbs)
+    bytesC = sum(10.0 * x["B"] * k_rows(x["n"]) * x["m"] for x in mbs)
+    flops = sum(float(x["B"] * gram_flops(k_rows(x["n"]), x["m"])) for x in mbs)
+    ph = {n: sum(pm[i] for pm in per_mb) for i, n in enumerate(names)}
+    phases = {
+        "momentum_keys": {"ms": ph["momentum_keys"], "GB/s": bytesA / ph["momentum_keys"] / 1e6,
+                          "frac_hbm": bytesA / ph["momentum_keys"] / 1e6 / hbm,
+                          "algorithmic_bytes": bytesA},
+        "select": {"ms": ph["select"]},
+        "gather": {"ms": ph["gather"], "GB/s": bytesC / ph["gather"] / 1e6, "frac_hbm": bytesC / ph["gather"] / 1e6 / hbm,
+                   "algorithmic_bytes": bytesC},
+        "gram_ns_products": {"ms": ph["gram_ns_products"], "TFLOP/s": flops / ph["gram_ns_products"] / 1e9,
+                             "frac_tensor_sustained": flops / ph["gram_ns_products"] / 1e9 / tc_sus,
+                             "useful_flops": flops},
+        "per_megabatch_ms": [{"shape": f"{x['B']}x{x['n']}x{x['m']}", "ms": sum(pm)} for x, pm in zip(mbs, per_mb)],
+    }
+    dominant = max(names, key=lambda n: ph[n])
+    launches_per_mb = d3.step_launch_count(T_ITERS, RESTARTS)
+    if dominant == "gram_ns_products":
+        n_launch = len(mbs) * (launches_per_mb - 3)
+        achieved = flops / ph[dominant] / 1e9
+        roof = {"kernel": "tc_gemm_kernel (all tcgen05 GEMM launches of the Gram-NS chain)", "bound": "tensor",
+                "achieved": achieved, "peak": tc_sus, "unit": "TFLOP/s", "frac": achieved / tc_sus,
+                "peak_source": f"{peaks_kind} bf16_tflops_sustained (fp16 dense rate = bf16 dense rate)",
+                "launches_per_step": n_launch, "per_launch_work": flops / n_launch}
+    else:
+        kernel_bytes = bytesA if dominant == "momentum_keys" else bytesC
+        achieved = kernel_bytes / ph[dominant] / 1e6
+        roof = {"kernel": dominant, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "peak_source": f"{peaks_kind} hbm_gbs",
+                "launches_per_step": len(mbs), "per_launch_work": kernel_bytes / len(mbs)}
+    roof["traffic"] = recorded_traffic(roof["kernel"])
+
+    line = {
+        "metric": METRIC,
+        "value": ms_rank / world,
+        "unit": "ms per megabatch step (both 7B shape groups)",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": ms_rank,
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "megabatches": [f"{b}x{n}x{m}" for b, n, m in MEGABATCHES],
+                   "l2": "inputs larger than L2 (about 65 GB touched per step)", "state": "W, M fp32; G bf16",
+                   "gram_iterates": "float16 (the paper's precision), fp32 accumulation",
+                   "parallelism": f"replica per GPU x{world} (independent megabatches, no collective)"},
+        "roofline": roof,
+        "phases": phases,
+        "gpu_launches": K * len(mbs) * launches_per_mb,
+        "clocks": clk,
+        "device_status": dev_status,
+        "wall_s_timed": wall1 - wall0,
+    }
+
+    # end to end: G from pinned host memory, selected rows back to the host, every step
+    line["e2e"] = run_e2e(torch, d3, mbs, ws, status, args, dev, dist)
+
+    del mbs, ws
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_sub:
+        line["gram_ns"] = bench_gram_ns(torch, d3, synthetic, dev, peaks, peaks_kind)
+        line["sym_gemm"] = bench_sym_gemm(torch, d3, synthetic, dev, peaks, peaks_kind)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(synthetic, torch)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def recorded_traffic(kernel: str):
+    """dram read+write bytes per launch from the committed ncu summary, if it was taken on the
+    current source of that kernel (matched by a hash of its source file); else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(kernel)
+    if not entry:
+        return None
+    src = os.path.join(ROOT, "matrix_orthogonalizing_optimizer_syrk_gb300", "csrc", entry["source"])
+    try:
+        with open(src, "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return entry["bytes_per_launch"] if h == entry.get("source_sha256_16") else None
+
+
+def run_e2e(torch, d3, mbs, ws, status, args, dev, dist):
+    host_G = [x["Gs"][0].to("cpu").pin_memory() for x in mbs]
+    dev_G = [x["Gs"][1] for x in mbs]  # the copy target (its previous contents are overwritten)
+    host_sel = [torch.empty(x["sel"].shape, dtype=torch.int32).pin_memory() for x in mbs]
+    h2d = sum(g.numel() * g.element_size() for g in host_G)
+    d2h = sum(s.numel() * s.element_size() for s in host_sel)
+
+    def one():
+        for x, hg, dg, hs in zip(mbs, host_G, dev_G, host_sel):
+            dg.copy_(hg, non_blocking=True)
+            d3.step(x["W"], x["M"], dg, f=F, mu=MU, eta=ETA, norm_p=1, abc=ABC, restart_after=RESTARTS,
+                    compute=torch.float16, sel_out=x["sel"], workspace=ws, status=status)
+            hs.copy_(x["sel"], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    K = max(1, args.steps)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    t0.record()
+    for _ in range(K):
+        one()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / K
+    if dist is not None:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return {"value": ms / world, "unit": "ms per megabatch step (both 7B shape groups)",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "path": "G copied from pinned host memory, dion3_step through the C ABI, selected rows copied back"}
+
+
+def _time_calls(torch, fn, reps, flush=None):
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def bench_gram_ns(torch, d3, synthetic, dev, peaks, peaks_kind):
+    """Gram NS on the 7B megabatches (f = 1): bf16 momenta, fp16 iterates, restarts after 2, 4."""
+    out = {"workload": "gram_ns on 128x4096x4096 + 96x4096x11008 bf16 low-rank+noise, T=5 Jordan, restarts 2,4, "
+                       "fp16 iterates", "batches": []}
+    total_ms, total_flops = 0.0, 0.0
+    idx0 = 0
+    for (B, n, m) in MEGABATCHES:
+        X = torch.empty((B, n, m), dtype=torch.bfloat16, device=dev)
+        for i in range(B):
+            synthetic.lowrank_plus_noise(n, m, 3000 + idx0 + i, dtype=torch.bfloat16, device=dev, out=X[i])
+        idx0 += B
+        O = torch.empty_like(X)
+        ws = torch.empty(d3.workspace_bytes_gram_ns(B, n, m, torch.bfloat16, torch.float16, len(RESTARTS)),
+                         dtype=torch.uint8, device=dev)
+        fn = lambda: d3.gram_ns(X, ABC, RESTARTS, compute=torch.float16, out=O, workspace=ws)  # noqa: E731
+        fn()
+        torch.cuda.synchronize()
+        ms = _time_calls(torch, fn, 3)
+        fl = float(B * gram_flops(n, m))
+        out["batches"].append({"shape": f"{B}x{n}x{m}", "ms": ms, "matrices_per_s": B / ms * 1e3,
+                               "TFLOP/s": fl / ms / 1e9})
+        total_ms += ms
+        total_flops += fl
+        del X, O, ws
+        torch.cuda.empty_cache()
+    peak = float(peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]))
+    out["matrices_per_s"] = sum(b for b, _, _ in MEGABATCHES) / total_ms * 1e3
+    out["TFLOP/s"] = total_flops / total_ms / 1e9
+    out["frac_tensor_burst"] = out["TFLOP/s"] / peak
+    out["peak_source"] = f"{peaks_kind} bf16_tflops"
+    return out
+
+
+def bench_sym_gemm(torch, d3, synthetic, dev, peaks, peaks_kind):
+    """D = A A^T (+ C): n in {1024..8192}, k in {n, 4n}; TFLOP/s on n^2 k useful FLOPs; L2 flushed."""
+    peak = float(peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]))
+    flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_buf.fill_(1)  # noqa: E731
+    rows = []
+    for n in (1024, 2048, 4096, 8192):
+        for kmul in (1, 4):
+            k = n * kmul
+            A = synthetic.gaussian((n, k), seed=2000 + n + k, std=k ** -0.5, dtype=torch.bfloat16, device=dev)
+            C = synthetic.symmetric_gaussian(n, seed=2100 + n, dtype=torch.bfloat16, device=dev)
+            D = torch.empty((n, n), dtype=torch.bfloat16, device=dev)
+            for beta in (0.0, 1.0):
+                ours = lambda: d3.sym_gemm(A, C=C if beta else None, beta=beta, out=D)  # noqa: E731
+                if beta:
+                    ref = lambda: torch.addmm(C, A, A.T, out=D)  # noqa: E731
+                else:
+                    ref = lambda: torch.matmul(A, A.T, out=D)  # noqa: E731
+                ours()
+                ref()
+                torch.cuda.synchronize()
+                t_ours = _time_calls(torch, ours, 5, flush)
+                t_ref = _time_calls(torch, ref, 5, flush)
+                tf = n * n * k / t_ours / 1e9
+                rows.append({"n": n, "k": k, "beta": beta, "ms": t_ours, "TFLOP/s": tf, "frac": tf / peak,
+                             "torch_matmul_ms": t_ref, "speedup_vs_torch_matmul": t_ref / t_ours})
+            del A, C, D
+    head = [r for r in rows if r["n"] == 8192 and r["k"] == 32768 and r["beta"] == 0.0][0]
+    return {"workload": "sym_gemm bf16, fp32 accumulate, n in {1024,2048,4096,8192}, k in {n,4n}, beta in {0,1}",
+            "headline": {"n": 8192, "k": 32768, "TFLOP/s": head["TFLOP/s"], "frac": head["frac"]},
+            "peak": peak, "peak_source": f"{peaks_kind} bf16_tflops (kernel timed alone)", "sweep": rows}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def cpu_sample_inputs(synthetic, torch):
+    """Matrix 0 of each megabatch at the first timed step's state (M = 0), built on the host."""
+    import numpy as np
+
+    out = []
+    idx0 = 0
+    for (B, n, m) in MEGABATCHES:
+        W = synthetic.gaussian((n, m), seed=5000 + idx0, std=0.02, device="cpu").numpy()
+        G = synthetic.lowrank_plus_noise(n, m, 4000 + idx0, dtype=torch.bfloat16, device="cpu").float().numpy()
+        out.append((B, W, np.zeros((n, m), np.float32), G))
+        idx0 += B
+    return out
+
+
+def oracle_step_ms(samples) -> float:
+    """Oracle time for one Dion3 step of every megabatch, extrapolated from matrix 0 of each."""
+    import oracle
+
+    total = 0.0
+    for B, W, M, G in samples:
+        t0 = time.perf_counter()
+        oracle.dion3_step(W, M, G, F[0], F[1], mu=MU, eta=ETA, norm_p=1, abc=ABC, restart_after=RESTARTS)
+        total += (time.perf_counter() - t0) * B
+    return total * 1e3
+
+
+def cpu_baseline(synthetic, torch):
+    samples = cpu_sample_inputs(synthetic, torch)
+    ms = oracle_step_ms(samples)
+    return {"value": ms, "unit": "ms per megabatch step (both 7B shape groups)", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": "one oracle Dion3 step (float64, exact keys) on matrix 0 of each megabatch "
+                      "(4096x4096 and 4096x11008 at M=0), scaled by the megabatch sizes 128 and 96"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+
+    import synthetic
+
+    samples = cpu_sample_inputs(synthetic, torch)
+    for _ in range(args.warmup):
+        oracle_step_ms(samples)
+    t0 = time.perf_counter()
+    vals = [oracle_step_ms(samples) for _ in range(max(1, args.steps))]
+    wall = time.perf_counter() - t0
+    v = statistics.mean(vals)
+    cores = len(os.sched_getaffinity(0))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "ms per megabatch step (both 7B shape groups)",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": v, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "megabatches": [f"{b}x{n}x{m}" for b, n, m in MEGABATCHES]},
+        "cpu_baseline": {"value": v, "unit": "ms per megabatch step (both 7B shape groups)", "cores": cores,
+                         "kind": "oracle",
+                         "sample": "each step: one oracle Dion3 step on matrix 0 of each megabatch, scaled by 128 "
+                                   "and 96"},
+        "e2e": {"value": v, "unit": "ms per megabatch step (both 7B shape groups)", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "wall_s_timed": wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -185,6 +185,22 @@ int dion3_step(int batch, int n, int m,
                void* workspace, size_t workspace_bytes,
                int* status_dev, void* stream);
 
+/*
+ * dion3_step_timed -- dion3_step, and in addition records the caller's events (cudaEvent_t
+ * handles, created by the caller) on `stream` at the step's phase boundaries:
+ *   events[0] before the momentum pass, [1] after it, [2] after the row selection,
+ *   [3] after the gather of M[S,:], [4] after the Gram Newton-Schulz products (the end).
+ * Only the first n_events entries are used; NULL entries are skipped.  Use it to split a
+ * step's device time by phase.  (No counterpart on the pages: a measurement hook.)
+ */
+int dion3_step_timed(int batch, int n, int m,
+                     float* W, float* M, const void* G, int g_dtype,
+                     int f_num, int f_den, float mu, float eta, float wd, int norm_p,
+                     int T, const float* abc, const int* restart_after, int n_restart, float eps,
+                     int compute_dtype, int32_t* sel_out,
+                     void* workspace, size_t workspace_bytes,
+                     int* status_dev, void* stream, void* const* events, int n_events);
+
 /* Human-readable name of a return code. */
 const char* dion3_status_str(int code);
 

@@ -47,6 +47,9 @@ SIGNATURES = {
     "dion3_step": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_f, _c_f, _c_f,
                             _c_int, _c_int, ctypes.POINTER(_c_f), ctypes.POINTER(_c_int), _c_int, _c_f, _c_int,
                             _c_p, _c_p, _c_sz, _c_p, _c_p]),
+    "dion3_step_timed": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_f, _c_f,
+                                  _c_f, _c_int, _c_int, ctypes.POINTER(_c_f), ctypes.POINTER(_c_int), _c_int, _c_f,
+                                  _c_int, _c_p, _c_p, _c_sz, _c_p, _c_p, ctypes.POINTER(_c_p), _c_int]),
     "dion3_status_str": (ctypes.c_char_p, [_c_int]),
     "dion3_abi_version": (_c_int, []),
     "dion3_selftest_watchdog": (_c_int, [ctypes.c_longlong, _c_p, _c_p]),
@@ -215,8 +218,12 @@ def workspace_bytes_step(batch: int, n: int, m: int, f_num: int, f_den: int, nor
 def step(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, f=(1, 4), mu: float = 0.95, eta: float = 0.01,
          wd: float = 0.0, norm_p: int = 1, abc=None, restart_after=(2,), eps: float = 1e-7, compute=torch.float16,
          sel_out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-         status: torch.Tensor | None = None) -> torch.Tensor:
-    """One Dion3 step on [batch, n, m] (or [n, m]) contiguous W, M (fp32) and G; returns the selected rows."""
+         status: torch.Tensor | None = None, events=None) -> torch.Tensor:
+    """One Dion3 step on [batch, n, m] (or [n, m]) contiguous W, M (fp32) and G; returns the selected rows.
+
+    ``events``: optional list of up to five recorded-once ``torch.cuda.Event`` objects, recorded
+    by the library at the phase boundaries (see dion3_step_timed in include/dion3.h).
+    """
     for t, name in ((W, "W"), (M, "M"), (G, "G")):
         _cuda(t, name)
         if not t.is_contiguous():
@@ -237,10 +244,18 @@ def step(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, f=(1, 4), mu: float 
     need = workspace_bytes_step(batch, n, m, f_num, f_den, norm_p, compute, nr)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=M.device)
-    rc = lib().dion3_step(batch, n, m, _ptr(W), _ptr(M), _ptr(G), _dt(G), f_num, f_den, float(mu), float(eta),
-                          float(wd), norm_p, T, flat, rarr, nr, float(eps), _dtype_code(compute), _ptr(sel_out),
-                          _ptr(workspace), workspace.numel(), _ptr(status), _stream_ptr(M.device))
-    _check(rc, "dion3_step")
+    if events is None:
+        rc = lib().dion3_step(batch, n, m, _ptr(W), _ptr(M), _ptr(G), _dt(G), f_num, f_den, float(mu), float(eta),
+                              float(wd), norm_p, T, flat, rarr, nr, float(eps), _dtype_code(compute), _ptr(sel_out),
+                              _ptr(workspace), workspace.numel(), _ptr(status), _stream_ptr(M.device))
+        _check(rc, "dion3_step")
+    else:
+        handles = (_c_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+        rc = lib().dion3_step_timed(batch, n, m, _ptr(W), _ptr(M), _ptr(G), _dt(G), f_num, f_den, float(mu),
+                                    float(eta), float(wd), norm_p, T, flat, rarr, nr, float(eps),
+                                    _dtype_code(compute), _ptr(sel_out), _ptr(workspace), workspace.numel(),
+                                    _ptr(status), _stream_ptr(M.device), handles, len(events))
+        _check(rc, "dion3_step_timed")
     return sel_out
 
 
@@ -248,3 +263,28 @@ def selftest_watchdog(spin_limit_cycles: int, status: torch.Tensor) -> None:
     _cuda(status, "status")
     rc = lib().dion3_selftest_watchdog(int(spin_limit_cycles), _ptr(status), _stream_ptr(status.device))
     _check(rc, "dion3_selftest_watchdog")
+
+
+def gram_core_launch_count(T: int, restart_after=()) -> int:
+    """Kernel launches of the Gram Newton-Schulz product chain (mirrors the library's driver):
+    R_0; per iteration Z, Q Z (not right after a (re)start), then either the restart's Q X and
+    X X^T or, before the last iteration, the two R-update products; finally Q X."""
+    rs = set(int(r) for r in restart_after)
+    count, q_identity = 1, True
+    for t in range(1, T + 1):
+        count += 1
+        if q_identity:
+            q_identity = False
+        else:
+            count += 1
+        if t in rs:
+            count += 2
+            q_identity = True
+        elif t < T:
+            count += 2
+    return count + 1
+
+
+def step_launch_count(T: int, restart_after=()) -> int:
+    """Kernel launches of one dion3_step call: momentum pass, selection, gather, product chain."""
+    return 3 + gram_core_launch_count(T, restart_after)

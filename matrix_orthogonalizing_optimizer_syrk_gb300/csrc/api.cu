@@ -383,10 +383,25 @@ size_t dion3_step_workspace_bytes(int batch, int n, int m, int f_num, int f_den,
   return step_layout(batch, n, m, k, norm_p, compute_dtype, n_restart).total;
 }
 
+int dion3_step_timed(int batch, int n, int m, float* W, float* M, const void* G, int g_dtype, int f_num, int f_den,
+                     float mu, float eta, float wd, int norm_p, int T, const float* abc, const int* restart_after,
+                     int n_restart, float eps, int compute_dtype, int32_t* sel_out, void* workspace,
+                     size_t workspace_bytes, int* status_dev, void* stream, void* const* events, int n_events);
+
 int dion3_step(int batch, int n, int m, float* W, float* M, const void* G, int g_dtype, int f_num, int f_den,
                float mu, float eta, float wd, int norm_p, int T, const float* abc, const int* restart_after,
                int n_restart, float eps, int compute_dtype, int32_t* sel_out, void* workspace,
                size_t workspace_bytes, int* status_dev, void* stream) {
+  return dion3_step_timed(batch, n, m, W, M, G, g_dtype, f_num, f_den, mu, eta, wd, norm_p, T, abc, restart_after,
+                          n_restart, eps, compute_dtype, sel_out, workspace, workspace_bytes, status_dev, stream,
+                          nullptr, 0);
+}
+
+int dion3_step_timed(int batch, int n, int m, float* W, float* M, const void* G, int g_dtype, int f_num, int f_den,
+                     float mu, float eta, float wd, int norm_p, int T, const float* abc, const int* restart_after,
+                     int n_restart, float eps, int compute_dtype, int32_t* sel_out, void* workspace,
+                     size_t workspace_bytes, int* status_dev, void* stream, void* const* events, int n_events) {
+  if (n_events < 0 || (n_events > 0 && events == nullptr)) return DION3_EINVAL;
   if (batch < 0 || n < 0 || m < 0) return DION3_EINVAL;
   if (!dtype_valid(g_dtype) || !dtype_valid(compute_dtype)) return DION3_EINVAL;
   if (norm_p != 1 && norm_p != 2) return DION3_EINVAL;
@@ -433,13 +448,25 @@ int dion3_step(int batch, int n, int m, float* W, float* M, const void* G, int g
   sa.status = status_dev;
   if (wd == 0.f) sa.w_decay = 1.0f;
 
+  // Phase boundaries for the caller's timing events (0: start ... 4: end).
+  auto mark = [&](int i) {
+    if (i < n_events && events[i] != nullptr) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
+  };
+  mark(0);
   int rc = step_momentum_keys(sa, s);
   if (rc) return rc;
+  mark(1);
   rc = step_select(sa, s);
   if (rc) return rc;
-  if (k == 0) return DION3_OK;
+  mark(2);
+  if (k == 0) {
+    mark(3);
+    mark(4);
+    return DION3_OK;
+  }
   rc = step_gather(sa, s);
   if (rc) return rc;
+  mark(3);
   Core c;
   c.batch = batch;
   c.n = k;
@@ -460,7 +487,10 @@ int dion3_step(int batch, int n, int m, float* W, float* M, const void* G, int g
   c.w_rows = n;
   c.w_alpha = static_cast<float>(-eta_p);
   c.status = status_dev;
-  return run_core(c, s);
+  rc = run_core(c, s);
+  if (rc) return rc;
+  mark(4);
+  return DION3_OK;
 }
 
 int dion3_selftest_watchdog(long long spin_limit_cycles, int* status_dev, void* stream) {
