@@ -201,6 +201,28 @@ int dion3_step_timed(int batch, int n, int m,
                      void* workspace, size_t workspace_bytes,
                      int* status_dev, void* stream, void* const* events, int n_events);
 
+/*
+ * dion3_gram_ns_noalloc -- dion3_gram_ns for callers that cannot allocate device memory
+ * (no counterpart in the paper).  Same arguments and results as dion3_gram_ns, minus the
+ * workspace: the scratch comes from an array of DION3_NOALLOC_SCRATCH_BYTES compiled into the
+ * library, resident on every GPU that loads the library until the process exits.
+ *   - Sizes whose workspace (dion3_gram_ns_workspace_bytes, plus the copy of a misaligned X)
+ *     exceeds DION3_NOALLOC_SCRATCH_BYTES are rejected with DION3_EWORKSPACE, nothing enqueued.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current) and keeps it; make that first call before any stream capture.
+ *   - It allocates nothing and frees nothing.
+ *   - Every call uses the same array and leaves its contents behind; nothing in it needs to
+ *     start at zero.  Calls whose work overlaps on the GPU (other streams, other host
+ *     threads) race on the array: serialise them.
+ */
+#define DION3_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int dion3_gram_ns_noalloc(int batch, int n, int m,
+                          const void* X, int64_t ldx, int64_t strideX, int x_dtype,
+                          void* Out, int64_t ldo, int64_t strideO, int out_dtype,
+                          int T, const float* abc, const int* restart_after, int n_restart,
+                          float eps, int compute_dtype,
+                          int* status_dev, void* stream);
+
 /* Human-readable name of a return code. */
 const char* dion3_status_str(int code);
 

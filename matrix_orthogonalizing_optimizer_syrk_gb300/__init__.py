@@ -50,6 +50,9 @@ SIGNATURES = {
     "dion3_step_timed": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_f, _c_f,
                                   _c_f, _c_int, _c_int, ctypes.POINTER(_c_f), ctypes.POINTER(_c_int), _c_int, _c_f,
                                   _c_int, _c_p, _c_p, _c_sz, _c_p, _c_p, ctypes.POINTER(_c_p), _c_int]),
+    "dion3_gram_ns_noalloc": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_i64, _c_i64, _c_int, _c_p, _c_i64, _c_i64,
+                                       _c_int, _c_int, ctypes.POINTER(_c_f), ctypes.POINTER(_c_int), _c_int, _c_f,
+                                       _c_int, _c_p, _c_p]),
     "dion3_status_str": (ctypes.c_char_p, [_c_int]),
     "dion3_abi_version": (_c_int, []),
     "dion3_selftest_watchdog": (_c_int, [ctypes.c_longlong, _c_p, _c_p]),
@@ -288,3 +291,26 @@ def gram_core_launch_count(T: int, restart_after=()) -> int:
 def step_launch_count(T: int, restart_after=()) -> int:
     """Kernel launches of one dion3_step call: momentum pass, selection, gather, product chain."""
     return 3 + gram_core_launch_count(T, restart_after)
+
+
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024  # DION3_NOALLOC_SCRATCH_BYTES in include/dion3.h
+
+
+def gram_ns_noalloc(X: torch.Tensor, abc, restart_after=(), eps: float = 1e-7, compute=torch.float16,
+                    out: torch.Tensor | None = None, out_dtype=None, status: torch.Tensor | None = None) -> torch.Tensor:
+    """Gram Newton-Schulz without a caller workspace, for callers that may not allocate device
+    memory: the library uses its own fixed scratch array (NOALLOC_SCRATCH_BYTES per GPU).  The
+    output tensor must be provided when the caller cannot allocate; when ``out`` is None this
+    wrapper allocates it (for convenience in tests and scripts).  Calls share the scratch array,
+    so calls whose work overlaps on the GPU must be serialised."""
+    _cuda(X, "X")
+    batch, n, m, ldx, sx = _layout(X)
+    odt = (torch.float32 if compute == torch.float32 else X.dtype) if out_dtype is None else out_dtype
+    if out is None:
+        out = _empty_aligned(tuple(X.shape), odt, X.device)
+    _, _, _, ldo, so = _layout(_cuda(out, "out"))
+    T, flat, rarr, nr = _abc_arrays(abc, restart_after)
+    rc = lib().dion3_gram_ns_noalloc(batch, n, m, _ptr(X), ldx, sx, _dt(X), _ptr(out), ldo, so, _dt(out), T, flat,
+                                     rarr, nr, float(eps), _dtype_code(compute), _ptr(status), _stream_ptr(X.device))
+    _check(rc, "dion3_gram_ns_noalloc")
+    return out
