@@ -58,6 +58,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sub", action="store_true", help="skip the Gram-NS and sym-GEMM sub-measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--case", choices=["gram_small", "step_small", "sym_gemm"], default=None,
+                    help="run one small profiling case (a few GB, inputs larger than L2) instead of the bench")
     return ap.parse_args()
 
 
@@ -515,8 +517,44 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_case(args):
+    """Small, self-contained workloads for ncu captures (prints timings, not a bench line)."""
+    import torch
+
+    import matrix_orthogonalizing_optimizer_syrk_gb300 as d3
+    import synthetic
+    from matrix_orthogonalizing_optimizer_syrk_gb300 import _build
+
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    out = {"case": args.case}
+    if args.case == "gram_small":
+        B, n, m = 16, 1024, 4096  # 128 MB of bf16 input
+        X = synthetic.lowrank_batch(B, n, m, base_seed=7000, dtype=torch.bfloat16, device=dev)
+        fn = lambda: d3.gram_ns(X, ABC, RESTARTS, compute=torch.float16)  # noqa: E731
+    elif args.case == "step_small":
+        B, n, m = 16, 4096, 4096  # 1 GB of W and of M, 0.5 GB of G
+        W = synthetic.gaussian((B, n, m), seed=7100, std=0.02, device=dev)
+        M = torch.zeros((B, n, m), dtype=torch.float32, device=dev)
+        G = synthetic.lowrank_batch(B, n, m, base_seed=7200, dtype=torch.bfloat16, device=dev)
+        fn = lambda: d3.step(W, M, G, f=F, mu=MU, eta=ETA, abc=ABC, restart_after=RESTARTS)  # noqa: E731
+    else:
+        n, k = 8192, 16384  # 256 MB of bf16 input
+        A = synthetic.gaussian((n, k), seed=7300, std=k ** -0.5, dtype=torch.bfloat16, device=dev)
+        D = torch.empty((n, n), dtype=torch.bfloat16, device=dev)
+        fn = lambda: d3.sym_gemm(A, out=D)  # noqa: E731
+    fn()
+    torch.cuda.synchronize()
+    out["ms"] = _time_calls(torch, fn, 2)
+    print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.case:
+        run_case(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
