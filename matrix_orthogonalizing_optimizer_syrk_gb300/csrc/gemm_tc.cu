@@ -31,19 +31,26 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int EPI_WARPS = 4;
 constexpr long long DEFAULT_SPIN = 4000000000LL;  // clock cycles (about 2 s)
 
-template <int BN>
+// CL = 1: one CTA computes a 128 x BN tile.  CL = 2: a CTA pair computes a 256 x BN tile with
+// tcgen05.mma.cta_group::2 -- each CTA holds its 128 rows of A and half (BN / 2) of B, so
+// every SM stages and reads only half of the B tile.
+template <int BN, int CL>
 struct Cfg {
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int BAR_OFF = STAGES * (A_BYTES + B_BYTES);
+  static constexpr int B_BYTES = (BN / CL) * BK * 2;
+  static constexpr int STAGES = (196608 / (A_BYTES + B_BYTES)) < 8 ? (196608 / (A_BYTES + B_BYTES)) : 8;
+  // Epilogue staging: per epilogue warp, two buffers of {32x32 block, its transpose} in 16 bits.
+  static constexpr int STG_OFF = STAGES * (A_BYTES + B_BYTES);
+  static constexpr int STG_WARP = 2 * 2 * 2048;
+  static constexpr int BAR_OFF = STG_OFF + EPI_WARPS * STG_WARP;
   static constexpr int NBARS = 2 * STAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain
   static constexpr int SMEM = BAR_OFF + NBARS * 8 + 16 + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t TX_BYTES = CL * (A_BYTES + B_BYTES);  // what the MMA-issuing CTA waits for
 };
 
 struct KParams {
@@ -71,25 +78,46 @@ struct KParams {
 };
 
 // ----------------------------------------------------------------------------- tile order
-template <int EPI, int BN>
-__device__ __forceinline__ void decode_tile(const KParams& p, long long t, int& b, int& mi, int& nj) {
+// Work unit t -> (batch b, row block mi, column block nj).  With CL = 2 the unit is a pair of
+// row blocks (2q, 2q+1) sharing column block nj; CTA `rank` of the cluster takes row block
+// 2q + rank.
+template <int EPI, int BN, int CL>
+__device__ __forceinline__ void decode_tile(const KParams& p, long long t, uint32_t rank, int& b, int& mi, int& nj) {
   b = static_cast<int>(t / p.tiles_per_batch);
   int r = static_cast<int>(t - static_cast<long long>(b) * p.tiles_per_batch);
   if constexpr (EPI == EPI_SYM) {
-    // Row block i holds column blocks 0 .. i*BM/BN (the blocks that reach the lower triangle).
-    constexpr int RATIO = BN / BM;
-    int row = 0;
-    for (;;) {
-      const int c = row / RATIO + 1;
-      if (r < c) break;
-      r -= c;
-      ++row;
+    if constexpr (CL == 1) {
+      // Row block i holds column blocks 0 .. i*BM/BN (the blocks that reach the lower triangle).
+      constexpr int RATIO = BN / BM;
+      int row = 0;
+      for (;;) {
+        const int c = row / RATIO + 1;
+        if (r < c) break;
+        r -= c;
+        ++row;
+      }
+      mi = row;
+      nj = r;
+    } else {
+      // BN = 2 BM: row blocks 2q and 2q+1 both hold column blocks 0 .. q.
+      int q = 0;
+      for (;;) {
+        if (r < q + 1) break;
+        r -= q + 1;
+        ++q;
+      }
+      mi = 2 * q + static_cast<int>(rank);
+      nj = r;
     }
-    mi = row;
-    nj = r;
   } else {
-    mi = r % p.tiles_m;
-    nj = r / p.tiles_m;
+    if constexpr (CL == 1) {
+      mi = r % p.tiles_m;
+      nj = r / p.tiles_m;
+    } else {
+      const int P = (p.tiles_m + 1) / 2;
+      mi = 2 * (r % P) + static_cast<int>(rank);
+      nj = r / P;
+    }
   }
 }
 
@@ -237,6 +265,244 @@ __device__ __forceinline__ void epi_dispatch(const KParams& p, int b, int r, int
   }
 }
 
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+template <typename T>
+__device__ __forceinline__ float unpack_lo(uint32_t w) {
+  const uint16_t b = static_cast<uint16_t>(w & 0xFFFFu);
+  return Out<T>::ld(reinterpret_cast<const T*>(&b));
+}
+template <typename T>
+__device__ __forceinline__ float unpack_hi(uint32_t w) {
+  const uint16_t b = static_cast<uint16_t>(w >> 16);
+  return Out<T>::ld(reinterpret_cast<const T*>(&b));
+}
+
+// 32 consecutive C values of row r starting at c0, packed in pairs (zeros where out of range).
+template <typename T>
+__device__ __forceinline__ void load_c32(const KParams& p, const T* crow, int c0, uint32_t (&w)[16]) {
+  if (crow == nullptr) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = 0u;
+    return;
+  }
+  if (c0 + 31 < p.N && aligned16(crow + c0)) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(crow + c0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = s4[q];
+      w[4 * q + 0] = u.x;
+      w[4 * q + 1] = u.y;
+      w[4 * q + 2] = u.z;
+      w[4 * q + 3] = u.w;
+    }
+  } else {
+    const uint16_t* c16 = reinterpret_cast<const uint16_t*>(crow);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t lo = (c0 + 2 * i < p.N) ? c16[c0 + 2 * i] : 0u;
+      const uint32_t hi = (c0 + 2 * i + 1 < p.N) ? c16[c0 + 2 * i + 1] : 0u;
+      w[i] = lo | (hi << 16);
+    }
+  }
+}
+
+// Byte offset of element (row, col) in a 32 x 32 block of 16-bit values laid out the way a
+// TMA box of {32, 32} with 64-byte swizzle expects it: 64-byte rows, 16-byte units permuted
+// by (row / 2) mod 4.
+__device__ __forceinline__ uint32_t stg_off(int row, int col) {
+  return static_cast<uint32_t>(row * 64 + ((((col >> 3) ^ (row >> 1)) & 3) << 4) + ((col & 7) << 1));
+}
+
+// Epilogue of one tile for a 16-bit D (EPI_SYM or EPI_GEN).  Each warp owns 32 rows; every
+// 32-column chunk is converted, written into a swizzled staging block (and, for blocks below
+// the diagonal, into a transposed block: lane pairs exchange halves so every shared store is a
+// full word), and stored with TMA bulk stores.  A diagonal block is made exactly symmetric in
+// shared memory (its upper half copied from the transposed lower half) and stored once.
+// Chunks whose columns lie entirely above the warp's rows are skipped; TMA clips rows and
+// columns outside the matrix, and a warp whose rows all lie outside stores nothing.
+template <typename T, int BN, int EPI>
+__device__ __forceinline__ void epi_tile_tma(const KParams& p, const CUtensorMap* tmD, uint8_t* stg, int& buf,
+                                             uint32_t t_acc, int b, int mi, int nj, int ew, int lane, float ab) {
+  const int r0w = mi * BM + ew * 32;
+  const int r = r0w + lane;
+  const T* crow = nullptr;
+  if (EPI == EPI_SYM && p.beta != 0.f && r < p.M)
+    crow = static_cast<const T*>(p.C) + static_cast<long long>(b) * p.sC + static_cast<long long>(r) * p.ldc;
+  int nch = 0;
+  for (int ch = 0; r0w < p.M && ch < BN / 32; ++ch) {
+    const int c0 = nj * BN + ch * 32;
+    if (c0 >= p.N || (EPI == EPI_SYM && c0 > r0w)) break;
+    ++nch;
+  }
+  uint32_t cnx[16];
+  if (EPI == EPI_SYM && nch > 0) load_c32<T>(p, crow, nj * BN, cnx);
+#pragma unroll 1
+  for (int ch = 0; ch < nch; ++ch) {
+    const int c0 = nj * BN + ch * 32;
+    uint32_t cw[16];
+    if (EPI == EPI_SYM) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) cw[i] = cnx[i];
+      if (ch + 1 < nch) load_c32<T>(p, crow, c0 + 32, cnx);  // prefetch the next chunk's C
+    }
+    uint32_t v[32];
+    __syncwarp();
+    if (p.num_kb > 0) {
+      ptx::tmem_ld_32x32b_x32(t_acc + ch * 32, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0u;
+    }
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float lo = __uint_as_float(v[2 * i]) * ab;
+      float hi = __uint_as_float(v[2 * i + 1]) * ab;
+      if (EPI == EPI_SYM) {
+        if (p.beta != 0.f) {
+          lo = fmaf(p.beta, unpack_lo<T>(cw[i]), lo);
+          hi = fmaf(p.beta, unpack_hi<T>(cw[i]), hi);
+        }
+        if (p.gamma != 0.f) {
+          if (c0 + 2 * i == r) lo += p.gamma;
+          if (c0 + 2 * i + 1 == r) hi += p.gamma;
+        }
+      }
+      w[i] = pack2<T>(lo, hi);
+    }
+    const bool diag = (EPI == EPI_SYM) && (c0 == r0w);
+    const bool below = (EPI == EPI_SYM) && (c0 < r0w);
+    // the buffer used two chunks ago must have been read by its TMA store
+    if (lane == 0) ptx::bulk_wait_read_le1();
+    __syncwarp();
+    uint8_t* S = stg + buf * 4096;
+    uint8_t* Tt = S + 2048;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(S + lane * 64 + ((((q) ^ (lane >> 1)) & 3) << 4)) =
+          make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    if (diag || below) {
+      const bool odd = lane & 1;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t s0 = odd ? (w[2 * j] & 0xFFFFu) : (w[2 * j] >> 16);
+        const uint32_t s1 = odd ? (w[2 * j + 1] & 0xFFFFu) : (w[2 * j + 1] >> 16);
+        const uint32_t rcv = __shfl_xor_sync(0xffffffffu, s0 | (s1 << 16), 1);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int k = 2 * j + h;
+          const uint32_t rk = h ? (rcv >> 16) : (rcv & 0xFFFFu);
+          const uint32_t word = odd ? (rk | (w[k] & 0xFFFF0000u)) : ((w[k] & 0xFFFFu) | (rk << 16));
+          const int c = 2 * k + (odd ? 1 : 0);
+          *reinterpret_cast<uint32_t*>(Tt + c * 64 + ((((lane >> 3) ^ (c >> 1)) & 3) << 4) + (((lane >> 1) & 3) << 2)) =
+              word;
+        }
+      }
+      if (diag) {
+        __syncwarp();
+        for (int c = lane + 1; c < 32; ++c)
+          *reinterpret_cast<uint16_t*>(S + stg_off(lane, c)) = *reinterpret_cast<const uint16_t*>(Tt + stg_off(lane, c));
+      }
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      ptx::tma_store_3d(tmD, ptx::smem_u32(S), c0, r0w, b);
+      if (below) ptx::tma_store_3d(tmD, ptx::smem_u32(Tt), r0w, c0, b);
+      ptx::bulk_commit_group();
+    }
+    buf ^= 1;
+  }
+}
+
+// 32 fp32 values of W starting at column c0 of `wrow` (zeros outside the matrix).
+__device__ __forceinline__ void load_w32(const float* wrow, int c0, int N, float4 (&x)[8]) {
+  if (wrow != nullptr && c0 + 31 < N && aligned16(wrow + c0)) {
+    const float4* s4 = reinterpret_cast<const float4*>(wrow + c0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = s4[i];
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = c0 + 4 * i;
+      x[i].x = (wrow && c < N) ? wrow[c] : 0.f;
+      x[i].y = (wrow && c + 1 < N) ? wrow[c + 1] : 0.f;
+      x[i].z = (wrow && c + 2 < N) ? wrow[c + 2] : 0.f;
+      x[i].w = (wrow && c + 3 < N) ? wrow[c + 3] : 0.f;
+    }
+  }
+}
+
+// Epilogue of the fused row update W[sel[r], :] += alpha * acc: the W segment of this warp's
+// next chunk is loaded while the current one is added and stored, so the read latency of the
+// scattered rows is not on the critical path of every chunk.
+template <int BN>
+__device__ __forceinline__ void epi_tile_wupd(const KParams& p, uint32_t t_acc, int b, int mi, int nj, int ew,
+                                              int lane, float ab) {
+  const int r0w = mi * BM + ew * 32;
+  if (r0w >= p.M) return;
+  const int r = r0w + lane;
+  float* wrow = nullptr;
+  if (r < p.M) {
+    const int row = __ldg(p.sel + static_cast<long long>(b) * p.ssel + r);
+    if (row >= 0 && row < p.w_rows)  // only a failed selection leaves rows outside [0, w_rows)
+      wrow = p.W + static_cast<long long>(b) * p.sW + static_cast<long long>(row) * p.ldw;
+  }
+  int nch = 0;
+  while (nch < BN / 32 && nj * BN + nch * 32 < p.N) ++nch;
+  float4 nx[8];
+  if (nch > 0) load_w32(wrow, nj * BN, p.N, nx);
+#pragma unroll 1
+  for (int ch = 0; ch < nch; ++ch) {
+    const int c0 = nj * BN + ch * 32;
+    float4 x[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = nx[i];
+    if (ch + 1 < nch) load_w32(wrow, c0 + 32, p.N, nx);
+    uint32_t v[32];
+    __syncwarp();
+    if (p.num_kb > 0) {
+      ptx::tmem_ld_32x32b_x32(t_acc + ch * 32, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0u;
+    }
+    if (wrow == nullptr) continue;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      x[i].x = fmaf(__uint_as_float(v[4 * i + 0]), ab, x[i].x);
+      x[i].y = fmaf(__uint_as_float(v[4 * i + 1]), ab, x[i].y);
+      x[i].z = fmaf(__uint_as_float(v[4 * i + 2]), ab, x[i].z);
+      x[i].w = fmaf(__uint_as_float(v[4 * i + 3]), ab, x[i].w);
+    }
+    if (c0 + 31 < p.N && aligned16(wrow + c0)) {
+      float4* d4 = reinterpret_cast<float4*>(wrow + c0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) d4[i] = x[i];
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = c0 + 4 * i;
+        if (c < p.N) wrow[c] = x[i].x;
+        if (c + 1 < p.N) wrow[c + 1] = x[i].y;
+        if (c + 2 < p.N) wrow[c + 2] = x[i].z;
+        if (c + 3 < p.N) wrow[c + 3] = x[i].w;
+      }
+    }
+  }
+}
+
 // Wait that ignores the abort flag (used while draining after an abort), bounded by time.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long limit) {
   const long long t0 = clock64();
@@ -246,11 +512,11 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long l
 }
 
 // ----------------------------------------------------------------------------- kernel
-template <int BN, bool B_MN, int EPI>
+template <int BN, bool B_MN, int EPI, int CL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const KParams p) {
-  using Cf = Cfg<BN>;
+                   const __grid_constant__ CUtensorMap tmD, const KParams p) {
+  using Cf = Cfg<BN, CL>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -267,6 +533,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tempty0 = tfull0 + 16;
   const uint32_t drain_bar = tempty0 + 16;
 
+  const uint32_t rank = CL == 2 ? ptx::cluster_ctarank() : 0u;
+  const bool leader = rank == 0;  // the CTA that issues the MMAs (CL = 2: the even CTA)
+  const long long unit0 = blockIdx.x / CL, unit_step = gridDim.x / CL;
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cf::STAGES; ++s) {
       ptx::mbar_init(full0 + 8 * s, 1);
@@ -274,20 +543,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(tfull0 + 8 * a, 1);
-      ptx::mbar_init(tempty0 + 8 * a, 4);
+      ptx::mbar_init(tempty0 + 8 * a, EPI_WARPS * CL);  // every epilogue warp of the pair releases it
     }
     ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmB);
+    if (EPI != EPI_WUPD && p.d_type != FP32) ptx::tma_prefetch_desc(&tmD);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_holder), Cf::TMEM_COLS);
-    ptx::tmem_relinquish();
+    if constexpr (CL == 2) {
+      ptx::tmem_alloc_pair(ptx::smem_u32(tmem_holder), Cf::TMEM_COLS);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_u32(tmem_holder), Cf::TMEM_COLS);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if (CL == 2) ptx::cluster_sync();  // both CTAs' barriers exist before either signals the other
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   volatile int* abort = abort_flag;
@@ -300,24 +576,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       uint32_t filled = 0, fill_parity = 0;
       bool ok = true;
-      for (long long t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
+      for (long long t = unit0; ok && t < p.total_tiles; t += unit_step) {
         int b, mi, nj;
-        decode_tile<EPI, BN>(p, t, b, mi, nj);
+        decode_tile<EPI, BN, CL>(p, t, rank, b, mi, nj);
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!ptx::mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort, lim)) {
             ok = false;
             break;
           }
           const uint32_t fb = full0 + 8 * stage;
-          ptx::mbar_arrive_expect_tx(fb, Cf::TX_BYTES);
-          ptx::tma_load_3d(ptx::smem_u32(sA + stage * Cf::A_BYTES), &tmA, fb, kb * BK, mi * BM, b);
+          const uint32_t adst = ptx::smem_u32(sA + stage * Cf::A_BYTES);
           const uint32_t bdst = ptx::smem_u32(sB + stage * Cf::B_BYTES);
-          if constexpr (!B_MN) {
-            ptx::tma_load_3d(bdst, &tmB, fb, kb * BK, nj * BN, b);
-          } else {
+          if constexpr (CL == 1) {
+            ptx::mbar_arrive_expect_tx(fb, Cf::TX_BYTES);
+            ptx::tma_load_3d(adst, &tmA, fb, kb * BK, mi * BM, b);
+            if constexpr (!B_MN) {
+              ptx::tma_load_3d(bdst, &tmB, fb, kb * BK, nj * BN, b);
+            } else {
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c)
-              ptx::tma_load_3d(bdst + c * (BK * 128), &tmB, fb, nj * BN + c * 64, kb * BK, b);
+              for (int c = 0; c < BN / 64; ++c)
+                ptx::tma_load_3d(bdst + c * (BK * 128), &tmB, fb, nj * BN + c * 64, kb * BK, b);
+            }
+          } else {
+            // Each CTA stages its own 128 rows of A and its half of B; all the bytes of the pair
+            // complete the even CTA's barrier, which the MMA issuer waits on.
+            const uint32_t fb_lead = ptx::mapa_shared(fb, 0);
+            if (leader) ptx::mbar_arrive_expect_tx(fb, Cf::TX_BYTES);
+            ptx::tma_load_3d_pair(adst, &tmA, fb_lead, kb * BK, mi * BM, b);
+            if constexpr (!B_MN) {
+              ptx::tma_load_3d_pair(bdst, &tmB, fb_lead, kb * BK, nj * BN + static_cast<int>(rank) * (BN / 2), b);
+            } else {
+#pragma unroll
+              for (int c = 0; c < BN / 128; ++c)
+                ptx::tma_load_3d_pair(bdst + c * (BK * 128), &tmB, fb_lead,
+                                      nj * BN + (static_cast<int>(rank) * (BN / 128) + c) * 64, kb * BK, b);
+            }
           }
           filled |= 1u << stage;
           fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
@@ -327,21 +620,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
-      if (!ok) {
-        // Let every issued copy land before the CTA's shared memory is released.
+      if (!ok && leader) {
+        // Let every issued copy land before the CTA's shared memory is released (in a pair,
+        // all copies complete the even CTA's barriers, and the final cluster barrier keeps
+        // the odd CTA alive until the even one has drained).
         for (int s = 0; s < Cf::STAGES; ++s)
           if (filled & (1u << s)) drain_wait(full0 + 8 * s, (fill_parity >> s) & 1u, lim);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       // ------------------------------------------------ MMA issuer
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (long long t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
+      for (long long t = unit0; ok && t < p.total_tiles; t += unit_step) {
         if (!ptx::mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, abort, lim)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -359,71 +654,111 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint64_t bd;
             if constexpr (!B_MN) bd = ptx::smem_desc_sw128(b_base + kk * 32, 16, 1024);
             else bd = ptx::smem_desc_sw128(b_base + kk * 16 * 128, BK * 128, 1024);
-            ptx::tc_mma_f16(d_tmem, ad, bd, p.idesc, (kb | kk) != 0 ? 1u : 0u);
+            if constexpr (CL == 2)
+              ptx::tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, (kb | kk) != 0 ? 1u : 0u);
+            else
+              ptx::tc_mma_f16(d_tmem, ad, bd, p.idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          ptx::tc_commit(empty0 + 8 * stage);
+          if constexpr (CL == 2)
+            ptx::tc_commit_pair_mc(empty0 + 8 * stage, 0x3);  // frees the stage in both CTAs
+          else
+            ptx::tc_commit(empty0 + 8 * stage);
           if (++stage == Cf::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        ptx::tc_commit(tfull0 + 8 * acc);
+        if constexpr (CL == 2)
+          ptx::tc_commit_pair_mc(tfull0 + 8 * acc, 0x3);  // both CTAs' epilogues may start
+        else
+          ptx::tc_commit(tfull0 + 8 * acc);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
       // Every MMA this thread issued has completed once the drain barrier fires.
-      ptx::tc_commit(drain_bar);
+      if constexpr (CL == 2)
+        ptx::tc_commit_pair(drain_bar);
+      else
+        ptx::tc_commit(drain_bar);
       drain_wait(drain_bar, 0, lim);
     }
   } else {
     // ------------------------------------------------ epilogue (warps 2..5)
     const int ew = warp & 3;  // TMEM lanes 32*ew .. 32*ew+31
+    uint8_t* stg = smem + Cf::STG_OFF + ew * Cf::STG_WARP;
+    int buf = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+    for (long long t = unit0; t < p.total_tiles; t += unit_step) {
       int b, mi, nj;
-      decode_tile<EPI, BN>(p, t, b, mi, nj);
+      decode_tile<EPI, BN, CL>(p, t, rank, b, mi, nj);
       if (!ptx::mbar_wait(tfull0 + 8 * acc, acc_phase, abort, lim)) break;
       ptx::tc_fence_after();
       const float ab = p.alpha * (p.alpha_batch ? __ldg(p.alpha_batch + b) : 1.f);
       const int r = mi * BM + ew * 32 + lane;
       const int rmax_warp = mi * BM + ew * 32 + 31;
       const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(acc * BN);
-#pragma unroll 1
-      for (int ch = 0; ch < BN / 32; ++ch) {
-        const int c0 = nj * BN + ch * 32;
-        if (c0 >= p.N) break;
-        if (EPI == EPI_SYM && c0 > rmax_warp) break;
-        uint32_t v[32];
-        __syncwarp();
-        if (p.num_kb > 0) {
-          ptx::tmem_ld_32x32b_x32(t_acc + ch * 32, v);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0u;
+      bool done = false;
+      if constexpr (EPI == EPI_WUPD) {
+        epi_tile_wupd<BN>(p, t_acc, b, mi, nj, ew, lane, ab);
+        done = true;
+      } else {
+        if (p.d_type != FP32) {
+          if (p.d_type == FP16)
+            epi_tile_tma<__half, BN, EPI>(p, &tmD, stg, buf, t_acc, b, mi, nj, ew, lane, ab);
+          else
+            epi_tile_tma<__nv_bfloat16, BN, EPI>(p, &tmD, stg, buf, t_acc, b, mi, nj, ew, lane, ab);
+          done = true;
         }
-        if (r < p.M) {
-          float a[32];
+      }
+      if (!done) {
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          const int c0 = nj * BN + ch * 32;
+          if (c0 >= p.N) break;
+          if (EPI == EPI_SYM && c0 > rmax_warp) break;
+          uint32_t v[32];
+          __syncwarp();
+          if (p.num_kb > 0) {
+            ptx::tmem_ld_32x32b_x32(t_acc + ch * 32, v);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) a[i] = __uint_as_float(v[i]) * ab;
-          epi_dispatch<EPI>(p, b, r, c0, a);
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
+          }
+          if (r < p.M) {
+            float a[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] = __uint_as_float(v[i]) * ab;
+            epi_dispatch<EPI>(p, b, r, c0, a);
+          }
         }
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(tempty0 + 8 * acc);
+      if (lane == 0) {
+        if (CL == 2)
+          ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty0 + 8 * acc, 0));
+        else
+          ptx::mbar_arrive(tempty0 + 8 * acc);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    // Every TMA store of this warp has finished before the CTA (and its staging) goes away.
+    if (lane == 0) ptx::bulk_wait_all();
   }
 
   __syncwarp();
   ptx::tc_fence_before();
   __syncthreads();
+  if (CL == 2) ptx::cluster_sync();  // no CTA leaves while its peer may still signal it
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, Cf::TMEM_COLS);
+    if constexpr (CL == 2)
+      ptx::tmem_dealloc_pair(tmem_base, Cf::TMEM_COLS);
+    else
+      ptx::tmem_dealloc(tmem_base, Cf::TMEM_COLS);
   }
   if (threadIdx.x == 0 && *abort && p.status) atomicOr(p.status, DION3_DEV_TIMEOUT);
 }
@@ -461,8 +796,10 @@ EncodeFn get_encode() {
   return fn;
 }
 
-// 3-D map over a 16-bit [batch][rows][cols] operand, box = box_cols x box_rows, 128-byte swizzle.
-bool make_map(CUtensorMap* map, const Mat& m, int rows, int cols, int batch, int box_cols, int box_rows) {
+// 3-D map over a 16-bit [batch][rows][cols] operand, box = box_cols x box_rows, 128-byte swizzle
+// (operand loads) or 64-byte swizzle (32 x 32 epilogue stores).
+bool make_map(CUtensorMap* map, const Mat& m, int rows, int cols, int batch, int box_cols, int box_rows,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeFn enc = get_encode();
   if (!enc) return false;
   const cuuint64_t es = 2;
@@ -476,13 +813,41 @@ bool make_map(CUtensorMap* map, const Mat& m, int rows, int cols, int batch, int
   cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType dt = m.dtype == FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUresult r = enc(map, dt, 3, const_cast<void*>(m.ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
+// Number of 2-CTA clusters of this kernel that fit on the device at once (cached per device).
 template <int BN, bool B_MN, int EPI>
+int max_clusters() {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  auto kern = tc_gemm_kernel<BN, B_MN, EPI, 2>;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<BN, 2>::SMEM;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = sm_count() / 2;
+  }
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+template <int BN, bool B_MN, int EPI, int CL>
 int launch(const GemmCall& g, cudaStream_t s) {
-  using Cf = Cfg<BN>;
+  using Cf = Cfg<BN, CL>;
   KParams p{};
   p.batch = g.batch;
   p.M = g.M;
@@ -490,16 +855,20 @@ int launch(const GemmCall& g, cudaStream_t s) {
   p.K = g.K;
   p.tiles_m = (g.M + BM - 1) / BM;
   p.tiles_n = (g.N + BN - 1) / BN;
+  const int pairs = (p.tiles_m + 1) / 2;
   if (EPI == EPI_SYM) {
     int cnt = 0;
-    for (int i = 0; i < p.tiles_m; ++i) cnt += i * BM / BN + 1;
+    if (CL == 1)
+      for (int i = 0; i < p.tiles_m; ++i) cnt += i * BM / BN + 1;
+    else
+      cnt = pairs * (pairs + 1) / 2;
     p.tiles_per_batch = cnt;
   } else {
-    p.tiles_per_batch = p.tiles_m * p.tiles_n;
+    p.tiles_per_batch = (CL == 1 ? p.tiles_m : pairs) * p.tiles_n;
   }
   p.total_tiles = static_cast<long long>(p.tiles_per_batch) * g.batch;
   p.num_kb = (g.K + BK - 1) / BK;
-  p.idesc = ptx::make_idesc_f16(g.A.dtype == FP16 ? 0 : 1, B_MN, BM, BN);
+  p.idesc = ptx::make_idesc_f16(g.A.dtype == FP16 ? 0 : 1, B_MN, BM * CL, BN);
   p.D = const_cast<void*>(g.D.ptr);
   p.ldd = g.D.ld;
   p.sD = g.D.stride;
@@ -534,16 +903,40 @@ int launch(const GemmCall& g, cudaStream_t s) {
   const int kdim = g.K > 0 ? g.K : 1;
   if (!make_map(&ta, Ae, g.M, kdim, g.batch, BK, BM)) return DION3_ECUDA;
   if (!B_MN) {
-    if (!make_map(&tb, Be, g.N, kdim, g.batch, BK, BN)) return DION3_ECUDA;
+    if (!make_map(&tb, Be, g.N, kdim, g.batch, BK, BN / CL)) return DION3_ECUDA;
   } else {
     if (!make_map(&tb, Be, kdim, g.N, g.batch, 64, BK)) return DION3_ECUDA;
   }
-  auto kern = tc_gemm_kernel<BN, B_MN, EPI>;
+  CUtensorMap td = ta;  // D as a TMA store target (16-bit D of EPI_SYM / EPI_GEN)
+  if (EPI != EPI_WUPD && g.D.dtype != FP32) {
+    if (!make_map(&td, g.D, g.M, g.N, g.batch, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return DION3_ECUDA;
+  }
+  auto kern = tc_gemm_kernel<BN, B_MN, EPI, CL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM) != cudaSuccess)
     return DION3_ECUDA;
-  long long grid = sm_count();
-  if (grid > p.total_tiles) grid = p.total_tiles;
-  kern<<<static_cast<unsigned>(grid), NUM_THREADS, Cf::SMEM, s>>>(ta, tb, p);
+  if constexpr (CL == 1) {
+    long long grid = sm_count();
+    if (grid > p.total_tiles) grid = p.total_tiles;
+    kern<<<static_cast<unsigned>(grid), NUM_THREADS, Cf::SMEM, s>>>(ta, tb, td, p);
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cf::SMEM;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(2 * max_clusters<BN, B_MN, EPI>(), 1, 1);
+    long long clusters = cfg.gridDim.x / 2;
+    if (clusters > p.total_tiles) clusters = p.total_tiles;
+    if (clusters < 1) clusters = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, td, p) != cudaSuccess) return DION3_ECUDA;
+  }
   return cudaGetLastError() == cudaSuccess ? DION3_OK : DION3_ECUDA;
 }
 
@@ -562,13 +955,17 @@ int sm_count() {
 
 int gemm_tc(const GemmCall& g, cudaStream_t s) {
   if (g.batch <= 0 || g.M <= 0 || g.N <= 0) return DION3_OK;
+  // Pairs of 128-row blocks share each 256-column B tile through cluster multicast when there
+  // are at least two row blocks; otherwise one CTA per tile.
   switch (g.epi) {
     case EPI_SYM:
-      return g.M <= 128 ? launch<128, false, EPI_SYM>(g, s) : launch<256, false, EPI_SYM>(g, s);
+      return g.M <= 128 ? launch<128, false, EPI_SYM, 1>(g, s) : launch<256, false, EPI_SYM, 2>(g, s);
     case EPI_GEN:
-      return g.N <= 128 ? launch<128, true, EPI_GEN>(g, s) : launch<256, true, EPI_GEN>(g, s);
+      if (g.N <= 128) return launch<128, true, EPI_GEN, 1>(g, s);
+      return g.M <= 128 ? launch<256, true, EPI_GEN, 1>(g, s) : launch<256, true, EPI_GEN, 2>(g, s);
     case EPI_WUPD:
-      return g.N <= 128 ? launch<128, true, EPI_WUPD>(g, s) : launch<256, true, EPI_WUPD>(g, s);
+      if (g.N <= 128) return launch<128, true, EPI_WUPD, 1>(g, s);
+      return g.M <= 128 ? launch<256, true, EPI_WUPD, 1>(g, s) : launch<256, true, EPI_WUPD, 2>(g, s);
     default:
       return DION3_EINVAL;
   }
