@@ -444,12 +444,15 @@ __device__ __forceinline__ void load_w32(const float* wrow, int c0, int N, float
   }
 }
 
-// Epilogue of the fused row update W[sel[r], :] += alpha * acc: the W segment of this warp's
-// next chunk is loaded while the current one is added and stored, so the read latency of the
-// scattered rows is not on the critical path of every chunk.
+// Epilogue of the fused row update W[sel[r], :] += alpha * acc.  Each lane streams 32 fp32
+// values (128 bytes) of its W row per chunk; with the chunk loop unrolled, the loads run three
+// chunks ahead of the adds and stores (about 3 x 4 KB in flight per warp), enough to cover
+// DRAM latency for these scattered rows.
 template <int BN>
 __device__ __forceinline__ void epi_tile_wupd(const KParams& p, uint32_t t_acc, int b, int mi, int nj, int ew,
                                               int lane, float ab) {
+  constexpr int NCH = BN / 32;
+  constexpr int AHEAD = 3;
   const int r0w = mi * BM + ew * 32;
   if (r0w >= p.M) return;
   const int r = r0w + lane;
@@ -459,45 +462,49 @@ __device__ __forceinline__ void epi_tile_wupd(const KParams& p, uint32_t t_acc, 
     if (row >= 0 && row < p.w_rows)  // only a failed selection leaves rows outside [0, w_rows)
       wrow = p.W + static_cast<long long>(b) * p.sW + static_cast<long long>(row) * p.ldw;
   }
-  int nch = 0;
-  while (nch < BN / 32 && nj * BN + nch * 32 < p.N) ++nch;
-  float4 nx[8];
-  if (nch > 0) load_w32(wrow, nj * BN, p.N, nx);
-#pragma unroll 1
-  for (int ch = 0; ch < nch; ++ch) {
+  float4 ring[AHEAD][8];
+#pragma unroll
+  for (int ch = 0; ch < AHEAD && ch < NCH; ++ch) {
+    if (nj * BN + ch * 32 < p.N) load_w32(wrow, nj * BN + ch * 32, p.N, ring[ch]);
+  }
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch) {
     const int c0 = nj * BN + ch * 32;
-    float4 x[8];
+    if (c0 < p.N) {
+      float4 x[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = nx[i];
-    if (ch + 1 < nch) load_w32(wrow, c0 + 32, p.N, nx);
-    uint32_t v[32];
-    __syncwarp();
-    if (p.num_kb > 0) {
-      ptx::tmem_ld_32x32b_x32(t_acc + ch * 32, v);
-    } else {
+      for (int i = 0; i < 8; ++i) x[i] = ring[ch % AHEAD][i];
+      if (ch + AHEAD < NCH && c0 + AHEAD * 32 < p.N) load_w32(wrow, c0 + AHEAD * 32, p.N, ring[ch % AHEAD]);
+      uint32_t v[32];
+      __syncwarp();
+      if (p.num_kb > 0) {
+        ptx::tmem_ld_32x32b_x32(t_acc + ch * 32, v);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = 0u;
-    }
-    if (wrow == nullptr) continue;
+        for (int i = 0; i < 32; ++i) v[i] = 0u;
+      }
+      if (wrow != nullptr) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      x[i].x = fmaf(__uint_as_float(v[4 * i + 0]), ab, x[i].x);
-      x[i].y = fmaf(__uint_as_float(v[4 * i + 1]), ab, x[i].y);
-      x[i].z = fmaf(__uint_as_float(v[4 * i + 2]), ab, x[i].z);
-      x[i].w = fmaf(__uint_as_float(v[4 * i + 3]), ab, x[i].w);
-    }
-    if (c0 + 31 < p.N && aligned16(wrow + c0)) {
-      float4* d4 = reinterpret_cast<float4*>(wrow + c0);
+        for (int i = 0; i < 8; ++i) {
+          x[i].x = fmaf(__uint_as_float(v[4 * i + 0]), ab, x[i].x);
+          x[i].y = fmaf(__uint_as_float(v[4 * i + 1]), ab, x[i].y);
+          x[i].z = fmaf(__uint_as_float(v[4 * i + 2]), ab, x[i].z);
+          x[i].w = fmaf(__uint_as_float(v[4 * i + 3]), ab, x[i].w);
+        }
+        if (c0 + 31 < p.N && aligned16(wrow + c0)) {
+          float4* d4 = reinterpret_cast<float4*>(wrow + c0);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) d4[i] = x[i];
-    } else {
+          for (int i = 0; i < 8; ++i) d4[i] = x[i];
+        } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int c = c0 + 4 * i;
-        if (c < p.N) wrow[c] = x[i].x;
-        if (c + 1 < p.N) wrow[c + 1] = x[i].y;
-        if (c + 2 < p.N) wrow[c + 2] = x[i].z;
-        if (c + 3 < p.N) wrow[c + 3] = x[i].w;
+          for (int i = 0; i < 8; ++i) {
+            const int c = c0 + 4 * i;
+            if (c < p.N) wrow[c] = x[i].x;
+            if (c + 1 < p.N) wrow[c + 1] = x[i].y;
+            if (c + 2 < p.N) wrow[c + 2] = x[i].z;
+            if (c + 3 < p.N) wrow[c + 3] = x[i].w;
+          }
+        }
       }
     }
   }
