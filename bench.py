@@ -302,6 +302,8 @@ def run_ours(args):
     if rank == 0 and not args.no_sub:
         line["gram_ns"] = bench_gram_ns(torch, d3, synthetic, dev, peaks, peaks_kind)
         line["sym_gemm"] = bench_sym_gemm(torch, d3, synthetic, dev, peaks, peaks_kind)
+        line["moe_step"] = bench_moe_step(torch, d3, synthetic, dev, peaks, peaks_kind)
+        line["gram_ns_fp32"] = bench_gram_fp32(torch, d3, synthetic, dev)
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(synthetic, torch)
     if rank == 0:
@@ -437,6 +439,64 @@ def bench_gram_ns(torch, d3, synthetic, dev, peaks, peaks_kind):
     out["frac_tensor_burst"] = out["TFLOP/s"] / peak
     out["peak_source"] = f"{peaks_kind} bf16_tflops"
     return out
+
+
+def bench_moe_step(torch, d3, synthetic, dev, peaks, peaks_kind):
+    """Dion3 step on a fine-grained MoE megabatch: 16 layers x 64 experts x {w1, w3, w2 oriented}
+    = 3072 matrices of 768 x 2048, f = 1/8 (k = 96, alpha' = 21.3), restarts after 2 and 4."""
+    B, n, m = 3072, 768, 2048
+    fk = (1, 8)
+    k = -((-n * fk[0]) // fk[1])
+    W = synthetic.gaussian((B, n, m), seed=6000, std=0.02, device=dev)
+    M = torch.zeros((B, n, m), dtype=torch.float32, device=dev)
+    Gs = [synthetic.lowrank_batch(B, n, m, base_seed=5000 + 10 ** 6 * s, dtype=torch.bfloat16, device=dev)
+          for s in range(2)]
+    ws = torch.empty(d3.workspace_bytes_step(B, n, m, fk[0], fk[1], 1, torch.float16, len(RESTARTS)),
+                     dtype=torch.uint8, device=dev)
+    sel = torch.empty((B, k), dtype=torch.int32, device=dev)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    for e in evs:
+        e.record()
+    state = {"s": 0}
+
+    def fn(events=None):
+        d3.step(W, M, Gs[state["s"] % 2], f=fk, mu=MU, eta=ETA, norm_p=1, abc=ABC, restart_after=RESTARTS,
+                compute=torch.float16, sel_out=sel, workspace=ws, events=events)
+        state["s"] += 1
+
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    ms = _time_calls(torch, fn, 5)
+    fn(evs)
+    torch.cuda.synchronize()
+    ph = [evs[i].elapsed_time(evs[i + 1]) for i in range(4)]
+    hbm = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
+    bytes_a = 10.0 * B * n * m
+    bytes_c = 10.0 * B * k * m
+    out = {"workload": "dion3_step f=1/8 on 3072 x 768x2048 (MoE experts), T=5 Jordan, restarts 2,4, fp16 iterates",
+           "ms": ms, "phases_ms": {"momentum_keys": ph[0], "select": ph[1], "gather": ph[2], "gram_ns_products": ph[3]},
+           "momentum_frac_hbm": bytes_a / ph[0] / 1e6 / hbm,
+           "hbm_floor_ms": (bytes_a + bytes_c) / hbm / 1e6,
+           "peak_source": f"{peaks_kind} hbm_gbs"}
+    del W, M, Gs, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_gram_fp32(torch, d3, synthetic, dev):
+    """fp32 Gram NS on one 256 x 1024 N(0,1) matrix from seed 0, restart after 2 (latency)."""
+    X = synthetic.gaussian((256, 1024), seed=0, device="cpu").to(dev)
+    X = X / X.norm()
+    ws = torch.empty(d3.workspace_bytes_gram_ns(1, 256, 1024, torch.float32, torch.float32, 1), dtype=torch.uint8,
+                     device=dev)
+    O = torch.empty_like(X)
+    fn = lambda: d3.gram_ns(X, ABC, (2,), compute=torch.float32, out=O, workspace=ws)  # noqa: E731
+    fn()
+    torch.cuda.synchronize()
+    ms = _time_calls(torch, fn, 20)
+    return {"workload": "gram_ns fp32 (FFMA) 256x1024, T=5 Jordan, restart after 2", "us": ms * 1e3,
+            "matrices_per_s": 1e3 / ms}
 
 
 def bench_sym_gemm(torch, d3, synthetic, dev, peaks, peaks_kind):
