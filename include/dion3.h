@@ -143,6 +143,38 @@ int dion3_gram_ns(int batch, int n, int m,
                   int* status_dev, void* stream);
 
 /*
+ * dion3_ns_standard_workspace_bytes -- bytes of device workspace dion3_ns_standard needs.
+ * Returns 0 for invalid sizes.
+ */
+size_t dion3_ns_standard_workspace_bytes(int batch, int n, int m, int compute_dtype);
+
+/*
+ * dion3_ns_standard -- Out = NS(X), the standard quintic Newton-Schulz iteration, for a batch
+ * of n x m matrices, 1 <= n <= m.  [D3] prerequisite "Newton-Schulz iteration" and [MB]
+ * "Doing an SVD without an SVD" define the iteration; [D3] "limitations" names it as the
+ * fallback for square matrices (alpha = 1), where Gram Newton-Schulz saves nothing and its
+ * restarts cost 3(alpha-1)n^3 = 0 anyway:
+ *   Xs = X / (||X||_F + eps);
+ *   for t = 1..T:  A = Xs Xs^T;  B = b_t A + c_t A^2;  Xs = a_t Xs + B Xs;
+ *   Out = Xs.
+ * A and B are symmetric products (lower triangle computed, mirrored); Xs = B Xs + a_t Xs is
+ * one general product with the a_t Xs term added in its epilogue, so an iteration costs
+ * (3 alpha + 1) n^3 useful FLOPs.  The iterates Xs, A, B are stored in compute_dtype (fp32
+ * accumulation).
+ *   X, Out, T, abc, eps, compute_dtype, workspace, status_dev, stream: as dion3_gram_ns (X is
+ *   always copied, prescaled, into the workspace).
+ *   Errors: EINVAL (n > m, T < 1), EWORKSPACE, EALIGN (Out, workspace), EUNSUPPORTED (fp32
+ *           compute with a 16-bit output), ECUDA.
+ *   Device: DION3_DEV_NONFINITE if a norm is not finite.
+ */
+int dion3_ns_standard(int batch, int n, int m,
+                      const void* X, int64_t ldx, int64_t strideX, int x_dtype,
+                      void* Out, int64_t ldo, int64_t strideO, int out_dtype,
+                      int T, const float* abc, float eps, int compute_dtype,
+                      void* workspace, size_t workspace_bytes,
+                      int* status_dev, void* stream);
+
+/*
  * dion3_k -- k = ceil(n * f_num / f_den) in exact integers ([D3] "existing work": k = ceil(f n)).
  * Returns -1 unless n >= 0 and 0 < f_num <= f_den.
  */
@@ -200,6 +232,29 @@ int dion3_step_timed(int batch, int n, int m,
                      int compute_dtype, int32_t* sel_out,
                      void* workspace, size_t workspace_bytes,
                      int* status_dev, void* stream, void* const* events, int n_events);
+
+/*
+ * dion3_step_dev -- dion3_step with the hyperparameters read on the device, for CUDA-graph
+ * capture: a graph captured around one call replays every later step with whatever values
+ * hyper_dev holds when it runs (a learning-rate schedule without re-capture).  [D3] "method
+ * details" Algorithm 4 (mu, eta, weight decay) and the step-time figures it reports for
+ * graph-captured optimizer steps.
+ *   hyper_dev : device float[3] = {mu, eta, wd}, 4-byte aligned, read by the kernels when they
+ *               run.  eta' = double(eta) * sqrt(f_den / f_num) and 1 - eta' wd are formed in
+ *               double and rounded once to fp32, exactly as dion3_step forms them on the host,
+ *               so both entry points give bit-identical results for the same values.
+ *   decay     : nonzero runs the W <- (1 - eta' wd) W pass (read-modify-write of all of W);
+ *               zero skips it whatever wd holds.  It is fixed at capture time.
+ *   Everything else as dion3_step.  The values are not checked for finiteness on the host.
+ *   Errors: as dion3_step; EINVAL if hyper_dev is NULL, EALIGN if it is not 4-byte aligned.
+ */
+int dion3_step_dev(int batch, int n, int m,
+                   float* W, float* M, const void* G, int g_dtype,
+                   int f_num, int f_den, const float* hyper_dev, int decay, int norm_p,
+                   int T, const float* abc, const int* restart_after, int n_restart, float eps,
+                   int compute_dtype, int32_t* sel_out,
+                   void* workspace, size_t workspace_bytes,
+                   int* status_dev, void* stream);
 
 /*
  * dion3_gram_ns_noalloc -- dion3_gram_ns for callers that cannot allocate device memory

@@ -42,6 +42,9 @@ SIGNATURES = {
     "dion3_gram_ns": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_i64, _c_i64, _c_int, _c_p, _c_i64, _c_i64, _c_int,
                                _c_int, ctypes.POINTER(_c_f), ctypes.POINTER(_c_int), _c_int, _c_f, _c_int,
                                _c_p, _c_sz, _c_p, _c_p]),
+    "dion3_ns_standard_workspace_bytes": (_c_sz, [_c_int, _c_int, _c_int, _c_int]),
+    "dion3_ns_standard": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_i64, _c_i64, _c_int, _c_p, _c_i64, _c_i64,
+                                   _c_int, _c_int, ctypes.POINTER(_c_f), _c_f, _c_int, _c_p, _c_sz, _c_p, _c_p]),
     "dion3_k": (_c_int, [_c_int, _c_int, _c_int]),
     "dion3_step_workspace_bytes": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "dion3_step": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_f, _c_f, _c_f,
@@ -50,6 +53,9 @@ SIGNATURES = {
     "dion3_step_timed": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_f, _c_f,
                                   _c_f, _c_int, _c_int, ctypes.POINTER(_c_f), ctypes.POINTER(_c_int), _c_int, _c_f,
                                   _c_int, _c_p, _c_p, _c_sz, _c_p, _c_p, ctypes.POINTER(_c_p), _c_int]),
+    "dion3_step_dev": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_p, _c_int,
+                                _c_int, _c_int, ctypes.POINTER(_c_f), ctypes.POINTER(_c_int), _c_int, _c_f, _c_int,
+                                _c_p, _c_p, _c_sz, _c_p, _c_p]),
     "dion3_gram_ns_noalloc": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_i64, _c_i64, _c_int, _c_p, _c_i64, _c_i64,
                                        _c_int, _c_int, ctypes.POINTER(_c_f), ctypes.POINTER(_c_int), _c_int, _c_f,
                                        _c_int, _c_p, _c_p]),
@@ -213,6 +219,38 @@ def gram_ns(X: torch.Tensor, abc, restart_after=(), eps: float = 1e-7, compute=t
     return out
 
 
+def workspace_bytes_ns_standard(batch: int, n: int, m: int, compute) -> int:
+    return int(lib().dion3_ns_standard_workspace_bytes(batch, n, m, _dtype_code(compute)))
+
+
+def ns_standard(X: torch.Tensor, abc, eps: float = 1e-7, compute=torch.float16, out: torch.Tensor | None = None,
+                out_dtype=None, workspace: torch.Tensor | None = None,
+                status: torch.Tensor | None = None) -> torch.Tensor:
+    """Standard quintic Newton-Schulz of each n x m matrix of X (n <= m): the fallback for
+    square matrices, where Gram Newton-Schulz saves nothing (Dion3 paper, limitations)."""
+    _cuda(X, "X")
+    batch, n, m, ldx, sx = _layout(X)
+    odt = (torch.float32 if compute == torch.float32 else X.dtype) if out_dtype is None else out_dtype
+    if out is None:
+        out = _empty_aligned(tuple(X.shape), odt, X.device)
+    _, _, _, ldo, so = _layout(_cuda(out, "out"))
+    T, flat, _, _ = _abc_arrays(abc, ())
+    need = workspace_bytes_ns_standard(batch, n, m, compute)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=X.device)
+    rc = lib().dion3_ns_standard(batch, n, m, _ptr(X), ldx, sx, _dt(X), _ptr(out), ldo, so, _dt(out), T, flat,
+                                 float(eps), _dtype_code(compute), _ptr(workspace), workspace.numel(), _ptr(status),
+                                 _stream_ptr(X.device))
+    _check(rc, "dion3_ns_standard")
+    return out
+
+
+def ns_standard_launch_count(T: int) -> int:
+    """Kernel launches of one dion3_ns_standard call: sum of squares, scale, cast, then three
+    products per iteration (plus a final cast when the output dtype differs)."""
+    return 3 + 3 * T
+
+
 def workspace_bytes_step(batch: int, n: int, m: int, f_num: int, f_den: int, norm_p: int, compute,
                          n_restart: int) -> int:
     return int(lib().dion3_step_workspace_bytes(batch, n, m, f_num, f_den, norm_p, _dtype_code(compute), n_restart))
@@ -221,11 +259,15 @@ def workspace_bytes_step(batch: int, n: int, m: int, f_num: int, f_den: int, nor
 def step(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, f=(1, 4), mu: float = 0.95, eta: float = 0.01,
          wd: float = 0.0, norm_p: int = 1, abc=None, restart_after=(2,), eps: float = 1e-7, compute=torch.float16,
          sel_out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-         status: torch.Tensor | None = None, events=None) -> torch.Tensor:
+         status: torch.Tensor | None = None, events=None, hyper: torch.Tensor | None = None,
+         decay: bool = False) -> torch.Tensor:
     """One Dion3 step on [batch, n, m] (or [n, m]) contiguous W, M (fp32) and G; returns the selected rows.
 
     ``events``: optional list of up to five recorded-once ``torch.cuda.Event`` objects, recorded
     by the library at the phase boundaries (see dion3_step_timed in include/dion3.h).
+    ``hyper``: optional fp32 device tensor {mu, eta, wd}; the kernels read it when they run
+    (``mu``, ``eta``, ``wd`` are then ignored and ``decay`` turns the W decay pass on), so the
+    call can be captured in a CUDA graph once and replayed with new values.
     """
     for t, name in ((W, "W"), (M, "M"), (G, "G")):
         _cuda(t, name)
@@ -247,7 +289,18 @@ def step(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, f=(1, 4), mu: float 
     need = workspace_bytes_step(batch, n, m, f_num, f_den, norm_p, compute, nr)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=M.device)
-    if events is None:
+    if hyper is not None:
+        _cuda(hyper, "hyper")
+        if hyper.dtype != torch.float32 or hyper.numel() < 3 or not hyper.is_contiguous():
+            raise ValueError("hyper must be a contiguous fp32 device tensor {mu, eta, wd}")
+        if events is not None:
+            raise ValueError("events and hyper cannot be combined")
+        rc = lib().dion3_step_dev(batch, n, m, _ptr(W), _ptr(M), _ptr(G), _dt(G), f_num, f_den, _ptr(hyper),
+                                  int(bool(decay)), norm_p, T, flat, rarr, nr, float(eps), _dtype_code(compute),
+                                  _ptr(sel_out), _ptr(workspace), workspace.numel(), _ptr(status),
+                                  _stream_ptr(M.device))
+        _check(rc, "dion3_step_dev")
+    elif events is None:
         rc = lib().dion3_step(batch, n, m, _ptr(W), _ptr(M), _ptr(G), _dt(G), f_num, f_den, float(mu), float(eta),
                               float(wd), norm_p, T, flat, rarr, nr, float(eps), _dtype_code(compute), _ptr(sel_out),
                               _ptr(workspace), workspace.numel(), _ptr(status), _stream_ptr(M.device))

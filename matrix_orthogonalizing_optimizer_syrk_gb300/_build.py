@@ -24,7 +24,10 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libdion3.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
+# Host code is compiled without floating-point contraction so that scalars derived on the host
+# (eta' = eta sqrt(1/f), 1 - eta' wd) round exactly like their device-side counterparts.
+NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
+              "--expt-relaxed-constexpr",
               "-I" + INCLUDE, "-I" + CSRC]
 
 

@@ -64,6 +64,29 @@ GramLayout gram_layout(int batch, int n, int m, bool need_copy, int cdt, int n_r
   return L;
 }
 
+// Standard Newton-Schulz: the prescaled X in two ping-pong buffers, A = X X^T and
+// B = b A + c A^2.
+struct NsLayout {
+  size_t rowsq, scale, X[2], A, B;
+  int64_t ldn, ldm;
+  size_t total;
+};
+
+NsLayout ns_layout(int batch, int n, int m, int cdt) {
+  NsLayout L{};
+  Carve cv;
+  const int es = dtype_size(cdt);
+  L.ldn = round_up(n, 8);
+  L.ldm = round_up(m, 8);
+  L.rowsq = cv.take(sizeof(float) * static_cast<size_t>(batch) * n);
+  L.scale = cv.take(sizeof(float) * batch);
+  for (int i = 0; i < 2; ++i) L.X[i] = cv.take(static_cast<size_t>(batch) * n * L.ldm * es);
+  L.A = cv.take(static_cast<size_t>(batch) * n * L.ldn * es);
+  L.B = cv.take(static_cast<size_t>(batch) * n * L.ldn * es);
+  L.total = round_up(static_cast<int64_t>(cv.off), WS_ALIGN);
+  return L;
+}
+
 struct StepLayout {
   size_t key_lo, key_hi, exact, rowsq, scale, xs;
   CoreLayout core;
@@ -117,6 +140,8 @@ struct Core {
   const int* sel = nullptr;
   int w_rows = 0;
   float w_alpha = 0.f;
+  const float* eta_dev = nullptr;  // when set, the W update's alpha is -double(*eta_dev) * eta_scale
+  double eta_scale = 0.0;
   int* status = nullptr;
 };
 
@@ -166,6 +191,10 @@ int run_core(const Core& c, cudaStream_t s) {
     g.sel = c.sel;
     g.ssel = c.n;
     g.w_rows = c.w_rows;
+    if (epi == EPI_WUPD) {
+      g.eta_dev = c.eta_dev;
+      g.eta_scale = c.eta_scale;
+    }
     g.status = c.status;
     return gemm(g, s);
   };
@@ -373,6 +402,90 @@ int dion3_gram_ns(int batch, int n, int m, const void* X, int64_t ldx, int64_t s
   return run_core(c, s);
 }
 
+size_t dion3_ns_standard_workspace_bytes(int batch, int n, int m, int compute_dtype) {
+  if (batch < 0 || n < 0 || m < n) return 0;
+  if (!dtype_valid(compute_dtype)) return 0;
+  return ns_layout(batch, n, m, compute_dtype).total;
+}
+
+int dion3_ns_standard(int batch, int n, int m, const void* X, int64_t ldx, int64_t strideX, int x_dtype, void* Out,
+                      int64_t ldo, int64_t strideO, int out_dtype, int T, const float* abc, float eps,
+                      int compute_dtype, void* workspace, size_t workspace_bytes, int* status_dev, void* stream) {
+  if (batch < 0 || n < 0 || m < 0) return DION3_EINVAL;
+  if (!dtype_valid(x_dtype) || !dtype_valid(out_dtype) || !dtype_valid(compute_dtype)) return DION3_EINVAL;
+  if (int rc = check_schedule(T, abc, nullptr, 0)) return rc;
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return DION3_EINVAL;
+  if (batch == 0 || n == 0) return DION3_OK;
+  if (n > m) return DION3_EINVAL;
+  if (compute_dtype == FP32 && out_dtype != FP32) return DION3_EUNSUPPORTED;
+  if (X == nullptr || Out == nullptr) return DION3_EINVAL;
+  if (ldx < m || ldo < m) return DION3_EINVAL;
+  if (batch > 1 && (strideX < n * ldx || strideO < n * ldo)) return DION3_EINVAL;
+  if (!al16(Out) || !ld_ok(ldo, out_dtype) || (batch > 1 && !ld_ok(strideO, out_dtype))) return DION3_EALIGN;
+  const NsLayout L = ns_layout(batch, n, m, compute_dtype);
+  if (workspace == nullptr || workspace_bytes < L.total) return DION3_EWORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & (WS_ALIGN - 1)) != 0) return DION3_EALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  float* rowsq = reinterpret_cast<float*>(ws + L.rowsq);
+  float* scale = reinterpret_cast<float*>(ws + L.scale);
+  const int64_t snm = static_cast<int64_t>(n) * L.ldm, snn = static_cast<int64_t>(n) * L.ldn;
+  const Mat Xb[2] = {Mat{ws + L.X[0], L.ldm, snm, compute_dtype}, Mat{ws + L.X[1], L.ldm, snm, compute_dtype}};
+  const Mat Am{ws + L.A, L.ldn, snn, compute_dtype}, Bm{ws + L.B, L.ldn, snn, compute_dtype};
+  const Mat Om{Out, ldo, strideO, out_dtype};
+  // The last product writes Out directly when Out has the compute dtype (the a X term is read
+  // in that dtype); otherwise it lands in a buffer that is converted at the end.
+  const bool direct = out_dtype == compute_dtype;
+
+  const Mat Xin{X, ldx, strideX, x_dtype};
+  int rc = rows_sumsq(batch, n, m, Xin, rowsq, status_dev, s);
+  if (rc) return rc;
+  rc = finalize_scale(batch, n, rowsq, eps, scale, nullptr, status_dev, s);
+  if (rc) return rc;
+  rc = scaled_cast(batch, n, m, Xin, scale, const_cast<void*>(Xb[0].ptr), L.ldm, snm, compute_dtype, s);
+  if (rc) return rc;
+  int cur = 0;
+  for (int t = 1; t <= T; ++t) {
+    const float a = abc[3 * (t - 1)], b = abc[3 * (t - 1) + 1], c = abc[3 * (t - 1) + 2];
+    GemmCall g;  // A = X X^T
+    g.batch = batch;
+    g.M = g.N = n;
+    g.K = m;
+    g.epi = EPI_SYM;
+    g.A = g.B = Xb[cur];
+    g.D = Am;
+    g.status = status_dev;
+    if ((rc = gemm(g, s))) return rc;
+    GemmCall h;  // B = c A A + b A
+    h.batch = batch;
+    h.M = h.N = h.K = n;
+    h.epi = EPI_SYM;
+    h.A = h.B = Am;
+    h.C = Am;
+    h.beta = b;
+    h.alpha = c;
+    h.D = Bm;
+    h.status = status_dev;
+    if ((rc = gemm(h, s))) return rc;
+    GemmCall u;  // X' = B X + a X
+    u.batch = batch;
+    u.M = n;
+    u.N = m;
+    u.K = n;
+    u.epi = EPI_GEN;
+    u.A = Bm;
+    u.B = Xb[cur];
+    u.C = Xb[cur];
+    u.beta = a;
+    u.D = (t == T && direct) ? Om : Xb[cur ^ 1];
+    u.status = status_dev;
+    if ((rc = gemm(u, s))) return rc;
+    cur ^= 1;
+  }
+  if (!direct) return scaled_cast(batch, n, m, Xb[cur], nullptr, Out, ldo, strideO, out_dtype, s);
+  return DION3_OK;
+}
+
 size_t dion3_step_workspace_bytes(int batch, int n, int m, int f_num, int f_den, int norm_p, int compute_dtype,
                                   int n_restart) {
   if (batch < 0 || n < 0 || m < n || n_restart < 0) return 0;
@@ -397,10 +510,17 @@ int dion3_step(int batch, int n, int m, float* W, float* M, const void* G, int g
                           nullptr, 0);
 }
 
-int dion3_step_timed(int batch, int n, int m, float* W, float* M, const void* G, int g_dtype, int f_num, int f_den,
-                     float mu, float eta, float wd, int norm_p, int T, const float* abc, const int* restart_after,
-                     int n_restart, float eps, int compute_dtype, int32_t* sel_out, void* workspace,
-                     size_t workspace_bytes, int* status_dev, void* stream, void* const* events, int n_events) {
+}  // extern "C"
+
+namespace {
+
+// One Dion3 step.  With hyper_dev == nullptr, mu, eta, wd are the host values; otherwise they
+// are read on the device from hyper_dev[0..2] and `decay` says whether the W decay pass runs.
+int step_impl(int batch, int n, int m, float* W, float* M, const void* G, int g_dtype, int f_num, int f_den,
+              float mu, float eta, float wd, const float* hyper_dev, bool decay, int norm_p, int T, const float* abc,
+              const int* restart_after, int n_restart, float eps, int compute_dtype, int32_t* sel_out,
+              void* workspace, size_t workspace_bytes, int* status_dev, void* stream, void* const* events,
+              int n_events) {
   if (n_events < 0 || (n_events > 0 && events == nullptr)) return DION3_EINVAL;
   if (batch < 0 || n < 0 || m < 0) return DION3_EINVAL;
   if (!dtype_valid(g_dtype) || !dtype_valid(compute_dtype)) return DION3_EINVAL;
@@ -415,12 +535,16 @@ int dion3_step_timed(int batch, int n, int m, float* W, float* M, const void* G,
   if (n > 16384 || m > 65536) return DION3_EUNSUPPORTED;
   if (W == nullptr || M == nullptr || G == nullptr || sel_out == nullptr) return DION3_EINVAL;
   if (!al16(W) || !al16(M) || !al16(G) || !al16(sel_out)) return DION3_EALIGN;
+  if (hyper_dev != nullptr && (reinterpret_cast<uintptr_t>(hyper_dev) & 3u) != 0) return DION3_EALIGN;
   const StepLayout L = step_layout(batch, n, m, k, norm_p, compute_dtype, n_restart);
   if (workspace == nullptr || workspace_bytes < L.total) return DION3_EWORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & (WS_ALIGN - 1)) != 0) return DION3_EALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  const double eta_p = static_cast<double>(eta) * std::sqrt(static_cast<double>(f_den) / f_num);
+  // eta' = eta / sqrt(f); double arithmetic, rounded once to fp32 where it is used.  The device
+  // path (hyper_dev) repeats exactly these operations on the value it reads.
+  const double eta_scale = std::sqrt(static_cast<double>(f_den) / static_cast<double>(f_num));
+  const double eta_p = static_cast<double>(eta) * eta_scale;
   const int64_t ldm = round_up(m, 8);
 
   StepArgs sa{};
@@ -434,7 +558,11 @@ int dion3_step_timed(int batch, int n, int m, float* W, float* M, const void* G,
   sa.g_dtype = g_dtype;
   sa.norm_p = norm_p;
   sa.mu = mu;
-  sa.w_decay = static_cast<float>(1.0 - eta_p * static_cast<double>(wd));
+  const double wd_term = eta_p * static_cast<double>(wd);
+  sa.w_decay = static_cast<float>(1.0 - wd_term);
+  sa.decay = hyper_dev != nullptr ? decay : (wd != 0.f && sa.w_decay != 1.0f);
+  sa.hyper = hyper_dev;
+  sa.eta_scale = eta_scale;
   sa.sel = sel_out;
   sa.key_lo = reinterpret_cast<float*>(ws + L.key_lo);
   sa.key_hi = reinterpret_cast<float*>(ws + L.key_hi);
@@ -446,7 +574,6 @@ int dion3_step_timed(int batch, int n, int m, float* W, float* M, const void* G,
   sa.scale = reinterpret_cast<float*>(ws + L.scale);
   sa.eps = eps;
   sa.status = status_dev;
-  if (wd == 0.f) sa.w_decay = 1.0f;
 
   // Phase boundaries for the caller's timing events (0: start ... 4: end).
   auto mark = [&](int i) {
@@ -486,11 +613,38 @@ int dion3_step_timed(int batch, int n, int m, float* W, float* M, const void* G,
   c.sel = sel_out;
   c.w_rows = n;
   c.w_alpha = static_cast<float>(-eta_p);
+  if (hyper_dev != nullptr) {
+    c.eta_dev = hyper_dev + 1;
+    c.eta_scale = eta_scale;
+  }
   c.status = status_dev;
   rc = run_core(c, s);
   if (rc) return rc;
   mark(4);
   return DION3_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dion3_step_timed(int batch, int n, int m, float* W, float* M, const void* G, int g_dtype, int f_num, int f_den,
+                     float mu, float eta, float wd, int norm_p, int T, const float* abc, const int* restart_after,
+                     int n_restart, float eps, int compute_dtype, int32_t* sel_out, void* workspace,
+                     size_t workspace_bytes, int* status_dev, void* stream, void* const* events, int n_events) {
+  return step_impl(batch, n, m, W, M, G, g_dtype, f_num, f_den, mu, eta, wd, nullptr, false, norm_p, T, abc,
+                   restart_after, n_restart, eps, compute_dtype, sel_out, workspace, workspace_bytes, status_dev,
+                   stream, events, n_events);
+}
+
+int dion3_step_dev(int batch, int n, int m, float* W, float* M, const void* G, int g_dtype, int f_num, int f_den,
+                   const float* hyper_dev, int decay, int norm_p, int T, const float* abc, const int* restart_after,
+                   int n_restart, float eps, int compute_dtype, int32_t* sel_out, void* workspace,
+                   size_t workspace_bytes, int* status_dev, void* stream) {
+  if (hyper_dev == nullptr) return DION3_EINVAL;
+  return step_impl(batch, n, m, W, M, G, g_dtype, f_num, f_den, 0.f, 0.f, 0.f, hyper_dev, decay != 0, norm_p, T,
+                   abc, restart_after, n_restart, eps, compute_dtype, sel_out, workspace, workspace_bytes, status_dev,
+                   stream, nullptr, 0);
 }
 
 int dion3_selftest_watchdog(long long spin_limit_cycles, int* status_dev, void* stream) {

@@ -57,7 +57,8 @@ __global__ void __launch_bounds__(256) rows_sumsq_kernel(int batch, int n, int m
   }
 }
 
-// Xc = X * scale[b], converted to the compute dtype (one warp per row).
+// Xc = X * scale[b] (scale == nullptr: a plain conversion), converted to Xc's dtype (one warp
+// per row).
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(256) scaled_cast_kernel(int batch, int n, int m, const Tin* X, long long ldx,
                                                           long long sx, const float* scale, Tout* Xc,
@@ -70,7 +71,7 @@ __global__ void __launch_bounds__(256) scaled_cast_kernel(int batch, int n, int 
     const long long b = row / n, i = row - b * n;
     const Tin* src = X + b * sx + i * ldx;
     Tout* dst = Xc + b * sc + i * ldc;
-    const float f = scale[b];
+    const float f = scale ? scale[b] : 1.f;
     for (int j = lane; j < m; j += 32) dst[j] = from_f<Tout>(to_f<Tin>(src[j]) * f);
   }
 }

@@ -32,6 +32,8 @@ struct SParams {
   const int* sel;
   long long ssel;
   int w_rows;
+  const float* eta_dev;
+  double eta_scale;
 };
 
 template <int TS, bool B_MN, int EPI>
@@ -114,7 +116,8 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SParams p) {
     if (kb + 1 < nkb) stash(buf ^ 1);
     __syncthreads();
   }
-  const float ab = p.alpha * (p.alpha_batch ? p.alpha_batch[b] : 1.f);
+  const float alpha = p.eta_dev ? __double2float_rn(-__dmul_rn(static_cast<double>(*p.eta_dev), p.eta_scale)) : p.alpha;
+  const float ab = alpha * (p.alpha_batch ? p.alpha_batch[b] : 1.f);
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const int r = mi * TS + ty * R + i;
@@ -133,6 +136,8 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SParams p) {
         D[static_cast<long long>(r) * p.ldd + c] = v;
         if (c < r) D[static_cast<long long>(c) * p.ldd + r] = v;
       } else if (EPI == EPI_GEN) {
+        if (p.beta != 0.f)
+          v = fmaf(p.beta, p.C[static_cast<long long>(b) * p.sC + static_cast<long long>(r) * p.ldc + c], v);
         p.D[static_cast<long long>(b) * p.sD + static_cast<long long>(r) * p.ldd + c] = v;
       } else {
         const int row = p.sel[static_cast<long long>(b) * p.ssel + r];
@@ -174,6 +179,8 @@ int launch(const GemmCall& g, cudaStream_t s) {
   p.sel = g.sel;
   p.ssel = g.ssel;
   p.w_rows = g.w_rows;
+  p.eta_dev = g.eta_dev;
+  p.eta_scale = g.eta_scale;
   if (g.batch > 65535) return DION3_EUNSUPPORTED;
   dim3 grid(p.tiles_per_batch, g.batch);
   simt_gemm_kernel<TS, B_MN, EPI><<<grid, NT, 0, s>>>(p);

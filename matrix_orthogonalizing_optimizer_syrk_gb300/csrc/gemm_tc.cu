@@ -7,7 +7,8 @@
 //            polynomial epilogue, Q Z, R Z, (R Z) Z).  Only tiles that reach the lower
 //            triangle are computed; the epilogue stores each lower element and its mirror,
 //            so D[j][i] is bit-identical to D[i][j].
-//   EPI_GEN  D = alpha*A*B with B stored K x N (N contiguous, "MN-major"): Q X.
+//   EPI_GEN  D = alpha*A*B + beta*C with B stored K x N (N contiguous, "MN-major"): Q X, and
+//            the standard Newton-Schulz update X' = B X + a X.
 //   EPI_WUPD like EPI_GEN, but the epilogue adds alpha*acc into W[b][sel[b][r]][:] -- the
 //            Dion3 row update W[S,:] -= eta' O fused into the last product (Algorithm 4).
 //
@@ -75,6 +76,8 @@ struct KParams {
   int w_rows;
   int* status;
   long long spin_limit;
+  const float* eta_dev;
+  double eta_scale;
 };
 
 // ----------------------------------------------------------------------------- tile order
@@ -211,6 +214,12 @@ __device__ __forceinline__ void epi_sym(const KParams& p, int b, int r, int c0, 
 template <typename T>
 __device__ __forceinline__ void epi_gen(const KParams& p, int b, int r, int c0, float (&acc)[32]) {
   T* drow = static_cast<T*>(p.D) + static_cast<long long>(b) * p.sD + static_cast<long long>(r) * p.ldd;
+  if (p.beta != 0.f) {
+    const T* crow = static_cast<const T*>(p.C) + static_cast<long long>(b) * p.sC + static_cast<long long>(r) * p.ldc;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (c0 + i < p.N) acc[i] = fmaf(p.beta, Out<T>::ld(crow + c0 + i), acc[i]);
+  }
   T o[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) o[i] = Out<T>::cvt(acc[i]);
@@ -336,8 +345,9 @@ __device__ __forceinline__ void epi_tile_tma(const KParams& p, const CUtensorMap
                                              uint32_t t_acc, int b, int mi, int nj, int ew, int lane, float ab) {
   const int r0w = mi * BM + ew * 32;
   const int r = r0w + lane;
+  const bool use_c = p.beta != 0.f;  // D = alpha acc + beta C (C has D's type and layout)
   const T* crow = nullptr;
-  if (EPI == EPI_SYM && p.beta != 0.f && r < p.M)
+  if (use_c && r < p.M)
     crow = static_cast<const T*>(p.C) + static_cast<long long>(b) * p.sC + static_cast<long long>(r) * p.ldc;
   int nch = 0;
   for (int ch = 0; r0w < p.M && ch < BN / 32; ++ch) {
@@ -346,12 +356,12 @@ __device__ __forceinline__ void epi_tile_tma(const KParams& p, const CUtensorMap
     ++nch;
   }
   uint32_t cnx[16];
-  if (EPI == EPI_SYM && nch > 0) load_c32<T>(p, crow, nj * BN, cnx);
+  if (use_c && nch > 0) load_c32<T>(p, crow, nj * BN, cnx);
 #pragma unroll 1
   for (int ch = 0; ch < nch; ++ch) {
     const int c0 = nj * BN + ch * 32;
     uint32_t cw[16];
-    if (EPI == EPI_SYM) {
+    if (use_c) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) cw[i] = cnx[i];
       if (ch + 1 < nch) load_c32<T>(p, crow, c0 + 32, cnx);  // prefetch the next chunk's C
@@ -369,15 +379,13 @@ __device__ __forceinline__ void epi_tile_tma(const KParams& p, const CUtensorMap
     for (int i = 0; i < 16; ++i) {
       float lo = __uint_as_float(v[2 * i]) * ab;
       float hi = __uint_as_float(v[2 * i + 1]) * ab;
-      if (EPI == EPI_SYM) {
-        if (p.beta != 0.f) {
-          lo = fmaf(p.beta, unpack_lo<T>(cw[i]), lo);
-          hi = fmaf(p.beta, unpack_hi<T>(cw[i]), hi);
-        }
-        if (p.gamma != 0.f) {
-          if (c0 + 2 * i == r) lo += p.gamma;
-          if (c0 + 2 * i + 1 == r) hi += p.gamma;
-        }
+      if (use_c) {
+        lo = fmaf(p.beta, unpack_lo<T>(cw[i]), lo);
+        hi = fmaf(p.beta, unpack_hi<T>(cw[i]), hi);
+      }
+      if (EPI == EPI_SYM && p.gamma != 0.f) {
+        if (c0 + 2 * i == r) lo += p.gamma;
+        if (c0 + 2 * i + 1 == r) hi += p.gamma;
       }
       w[i] = pack2<T>(lo, hi);
     }
@@ -702,7 +710,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       decode_tile<EPI, BN, CL>(p, t, rank, b, mi, nj);
       if (!ptx::mbar_wait(tfull0 + 8 * acc, acc_phase, abort, lim)) break;
       ptx::tc_fence_after();
-      const float ab = p.alpha * (p.alpha_batch ? __ldg(p.alpha_batch + b) : 1.f);
+      const float alpha =
+          p.eta_dev ? __double2float_rn(-__dmul_rn(static_cast<double>(__ldg(p.eta_dev)), p.eta_scale)) : p.alpha;
+      const float ab = alpha * (p.alpha_batch ? __ldg(p.alpha_batch + b) : 1.f);
       const int r = mi * BM + ew * 32 + lane;
       const int rmax_warp = mi * BM + ew * 32 + 31;
       const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(acc * BN);
@@ -895,6 +905,8 @@ int launch(const GemmCall& g, cudaStream_t s) {
   p.w_rows = g.w_rows;
   p.status = g.status;
   p.spin_limit = g.spin_limit > 0 ? g.spin_limit : DEFAULT_SPIN;
+  p.eta_dev = g.eta_dev;
+  p.eta_scale = g.eta_scale;
   if (p.total_tiles == 0) return DION3_OK;
 
   CUtensorMap ta, tb;
@@ -962,6 +974,7 @@ int sm_count() {
 
 int gemm_tc(const GemmCall& g, cudaStream_t s) {
   if (g.batch <= 0 || g.M <= 0 || g.N <= 0) return DION3_OK;
+  if (g.beta != 0.f && (g.C.ptr == nullptr || g.C.dtype != g.D.dtype)) return DION3_EUNSUPPORTED;
   // Pairs of 128-row blocks share each 256-column B tile through cluster multicast when there
   // are at least two row blocks; otherwise one CTA per tile.
   switch (g.epi) {

@@ -28,7 +28,8 @@ enum Epi { EPI_SYM = 0, EPI_GEN = 1, EPI_WUPD = 2 };
 // One batched GEMM as the drivers see it.
 //   SYM : D[b] (M x M) = alpha_b * A[b] B[b]^T + beta * C[b] + gamma * I, lower tiles only,
 //         upper triangle mirrored.  A, B are K-major ([b][M][K]).
-//   GEN : D[b] (M x N) = alpha_b * A[b] B[b]; A is [b][M][K], B is [b][K][N] (N contiguous).
+//   GEN : D[b] (M x N) = alpha_b * A[b] B[b] + beta * C[b]; A is [b][M][K], B is [b][K][N]
+//         (N contiguous); C (read when beta != 0) has D's dtype.
 //   WUPD: like GEN, but instead of storing D the epilogue adds alpha_b * acc into
 //         W[b][sel[b][r]][c] (fp32 read-modify-write).
 // alpha_b = alpha * (alpha_batch ? alpha_batch[b] : 1).
@@ -49,6 +50,10 @@ struct GemmCall {
   int w_rows = 0;  // rows of each W matrix (bounds for sel entries)
   int* status = nullptr;
   long long spin_limit = 0;  // clock cycles for bounded waits; 0 = default
+  // When set, alpha is replaced on the device by float(-(double(*eta_dev) * eta_scale)): the W
+  // row update's -eta' read from device memory at run time.
+  const float* eta_dev = nullptr;
+  double eta_scale = 0.0;
 };
 
 // 16-bit inputs on the tcgen05 tensor cores (gemm_tc.cu).
@@ -68,7 +73,7 @@ int rows_sumsq(int batch, int n, int m, Mat X, float* rowsq, int* status, cudaSt
 // scale[b] = 1 / (sqrt(sum_i rowsq[b*rows + i]) + eps); alpha2[b] = scale[b]^2 (alpha2 may be null).
 int finalize_scale(int batch, int rows, const float* rowsq, float eps, float* scale, float* alpha2,
                    int* status, cudaStream_t s);
-// Xc[b] = scale[b] * X[b] in the compute dtype cdt (ld ldc, stride sc).
+// Xc[b] = scale[b] * X[b] in dtype cdt (ld ldc, stride sc); scale == nullptr converts only.
 int scaled_cast(int batch, int n, int m, Mat X, const float* scale, void* Xc, int64_t ldc, int64_t sc, int cdt,
                 cudaStream_t s);
 
@@ -81,7 +86,12 @@ struct StepArgs {
   int g_dtype;
   int norm_p;
   float mu;
-  float w_decay;  // 1 - eta' * wd (1 means: no decay pass)
+  float w_decay;  // 1 - eta' * wd
+  bool decay;     // run the W <- w_decay W pass
+  // When set, mu, eta, wd are read from hyper[0..2] on the device (mu and w_decay then come
+  // from there; eta' = double(eta) * eta_scale).
+  const float* hyper;
+  double eta_scale;
   int32_t* sel;
   float* key_lo;
   float* key_hi;

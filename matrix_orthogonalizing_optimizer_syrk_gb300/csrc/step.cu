@@ -66,6 +66,8 @@ struct AArgs {
   float* W;
   float w_decay;
   bool decay;
+  const float* hyper;  // device {mu, eta, wd}: w_decay = 1 - double(eta) eta_scale double(wd)
+  double eta_scale;
   bool keys;
   float* key_lo;
   float* key_hi;
@@ -80,6 +82,10 @@ __global__ void __launch_bounds__(256) momentum_keys_kernel(const AArgs a) {
   const long long w0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
   const int m = a.m;
+  const float w_decay =
+      a.hyper ? __double2float_rn(__dsub_rn(1.0, __dmul_rn(__dmul_rn(static_cast<double>(a.hyper[1]), a.eta_scale),
+                                                            static_cast<double>(a.hyper[2]))))
+              : a.w_decay;
   for (long long row = w0; row < a.rows; row += nw) {
     float* Mr = a.M + row * m;
     const TG* Gr = static_cast<const TG*>(a.G) + row * m;
@@ -101,10 +107,10 @@ __global__ void __launch_bounds__(256) momentum_keys_kernel(const AArgs a) {
         if (a.decay) {
           float4* w4 = reinterpret_cast<float4*>(Wr + j);
           float4 wa = w4[0], wb = w4[1];
-          wa.x = __fmul_rn(wa.x, a.w_decay); wa.y = __fmul_rn(wa.y, a.w_decay);
-          wa.z = __fmul_rn(wa.z, a.w_decay); wa.w = __fmul_rn(wa.w, a.w_decay);
-          wb.x = __fmul_rn(wb.x, a.w_decay); wb.y = __fmul_rn(wb.y, a.w_decay);
-          wb.z = __fmul_rn(wb.z, a.w_decay); wb.w = __fmul_rn(wb.w, a.w_decay);
+          wa.x = __fmul_rn(wa.x, w_decay); wa.y = __fmul_rn(wa.y, w_decay);
+          wa.z = __fmul_rn(wa.z, w_decay); wa.w = __fmul_rn(wa.w, w_decay);
+          wb.x = __fmul_rn(wb.x, w_decay); wb.y = __fmul_rn(wb.y, w_decay);
+          wb.z = __fmul_rn(wb.z, w_decay); wb.w = __fmul_rn(wb.w, w_decay);
           w4[0] = wa;
           w4[1] = wb;
         }
@@ -124,7 +130,7 @@ __global__ void __launch_bounds__(256) momentum_keys_kernel(const AArgs a) {
         const float x = __fadd_rn(Mr[j], gval<TG>(Gr[j]));
         Mr[j] = x;
         q2[0] = fmaf(x, x, q2[0]);
-        if (a.decay) Wr[j] = __fmul_rn(Wr[j], a.w_decay);
+        if (a.decay) Wr[j] = __fmul_rn(Wr[j], w_decay);
         if (a.keys) {
           bad |= !isfinite(x);
           const float t = NORM_P == 1 ? fabsf(x) : __fmul_rn(x, x);
@@ -435,6 +441,7 @@ struct CArgs {
   void* XS;
   long long ldx;
   float mu;
+  const float* mu_dev;  // when set, mu is read from here
   const float* scale;
 };
 
@@ -452,6 +459,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const CArgs a) {
   const int lane = threadIdx.x & 31;
   const long long w0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  const float mu = a.mu_dev ? *a.mu_dev : a.mu;
   for (long long row = w0; row < a.rows; row += nw) {
     const long long b = row / a.k;
     const int i = a.sel[row];
@@ -472,13 +480,13 @@ __global__ void __launch_bounds__(256) gather_kernel(const CArgs a) {
         } else {
           *reinterpret_cast<float4*>(dst + c) = make_float4(x.x * f, x.y * f, x.z * f, x.w * f);
         }
-        *s4 = make_float4(__fmul_rn(a.mu, x.x), __fmul_rn(a.mu, x.y), __fmul_rn(a.mu, x.z), __fmul_rn(a.mu, x.w));
+        *s4 = make_float4(__fmul_rn(mu, x.x), __fmul_rn(mu, x.y), __fmul_rn(mu, x.z), __fmul_rn(mu, x.w));
       }
     } else {
       for (int c = lane; c < a.m; c += 32) {
         const float x = src[c];
         dst[c] = cvt_out<TC>(x * f);
-        src[c] = __fmul_rn(a.mu, x);
+        src[c] = __fmul_rn(mu, x);
       }
     }
   }
@@ -528,7 +536,9 @@ int step_momentum_keys(const StepArgs& s, cudaStream_t st) {
   a.G = s.G;
   a.W = s.W;
   a.w_decay = s.w_decay;
-  a.decay = s.w_decay != 1.0f;
+  a.decay = s.decay;
+  a.hyper = s.hyper;
+  a.eta_scale = s.eta_scale;
   a.keys = s.k < s.n;
   a.key_lo = s.key_lo;
   a.key_hi = s.key_hi;
@@ -586,6 +596,7 @@ int step_gather(const StepArgs& s, cudaStream_t st) {
   c.XS = s.XS;
   c.ldx = s.ldx;
   c.mu = s.mu;
+  c.mu_dev = s.hyper;
   c.scale = s.scale;
   const bool vec = (s.m % 4 == 0) && aligned16(s.M) && (s.ldx % 8 == 0);
   switch (s.cdt) {

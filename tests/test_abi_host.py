@@ -147,3 +147,56 @@ def test_step_validation(L):
     assert _step(L, ws=NULL) == 3
     assert _step(L, mu=float("nan")) == 1
     assert _step(L, rs=(9,)) == 1
+
+
+def _ns(L, n=64, m=128, X=FAKE, ldx=128, Out=FAKE, ldo=128, T=5, abc=None, ws=FAKE, wsb=1 << 40, xt=0, ot=0, ct=0,
+        eps=1e-7, batch=1):
+    abc = _abc(T) if abc is None else abc
+    return L.dion3_ns_standard(batch, n, m, X, ldx, n * ldx, xt, Out, ldo, n * ldo, ot, T, abc, eps, ct, ws, wsb,
+                               NULL, NULL)
+
+
+def test_ns_standard_validation(L):
+    assert _ns(L, n=200, m=100, ldx=100, ldo=104) == 1     # n > m
+    assert _ns(L, T=0) == 1
+    assert _ns(L, X=NULL) == 1
+    assert _ns(L, Out=NULL) == 1
+    assert _ns(L, ldo=64) == 1                              # ldo < m
+    assert _ns(L, eps=float("nan")) == 1
+    assert _ns(L, ws=NULL) == 3
+    assert _ns(L, wsb=16) == 3
+    assert _ns(L, Out=FAKE_ODD) == 5
+    assert _ns(L, ldo=132) == 5                             # 264-byte rows of bf16
+    assert _ns(L, ct=2, ot=0) == 2                          # fp32 compute needs fp32 output
+    assert _ns(L, xt=9) == 1
+    nan_abc = (ctypes.c_float * 15)(*([float("nan")] * 15))
+    assert _ns(L, abc=nan_abc) == 1
+    assert _ns(L, n=0) == 0
+    assert _ns(L, batch=0) == 0
+
+
+def test_ns_standard_workspace_query(L):
+    a = d3.workspace_bytes_ns_standard(1, 64, 128, 0)
+    b = d3.workspace_bytes_ns_standard(2, 64, 128, 0)
+    c = d3.workspace_bytes_ns_standard(1, 64, 128, 2)
+    assert 0 < a < b and a < c and a % 256 == 0
+    assert d3.workspace_bytes_ns_standard(1, 65, 64, 0) == 0
+
+
+def test_step_dev_validation(L):
+    hyper = FAKE
+    r = (ctypes.c_int * 1)(2)
+
+    def call(hyper=hyper, **kw):
+        args = dict(n=64, m=128, W=FAKE, M=FAKE, G=FAKE, sel=FAKE, fn=1, fd=4, ws=FAKE, wsb=1 << 40)
+        args.update(kw)
+        return L.dion3_step_dev(1, args["n"], args["m"], args["W"], args["M"], args["G"], 0, args["fn"], args["fd"],
+                                hyper, 1, 1, 5, _abc(5), r, 1, 1e-7, 0, args["sel"], args["ws"], args["wsb"],
+                                NULL, NULL)
+
+    assert call(hyper=NULL) == 1
+    assert call(hyper=ctypes.c_void_p(0x10002)) == 5      # not 4-byte aligned
+    assert call(fn=0) == 1
+    assert call(W=NULL) == 1
+    assert call(ws=NULL) == 3
+    assert call(n=0) == 0
