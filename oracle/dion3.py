@@ -13,6 +13,11 @@ Sources (page title, section):
   The step takes the Muon-equivalent eta and applies eta' itself; the weight
   decay factor uses eta' as well.
 * Same page, "existing work": k = ceil(f n), rows taken as they are.
+* Same page, "limitations" and "future directions": choosing S at random
+  works about as well as the l1 rule, and a set S that does not depend on M
+  is what lets a data-parallel run synchronise only M[S, :].  ``rows``
+  passes such a caller-chosen S (e.g. drawn at random by the caller); the
+  step is otherwise unchanged.
 
 Readings where the pages are silent:
 
@@ -79,10 +84,19 @@ def top_k_rows(keys, k: int) -> np.ndarray:
     return np.array(sorted(order[:k]), dtype=np.int64)
 
 
+def given_rows(rows, n: int, k: int) -> np.ndarray:
+    """A caller-chosen S: k distinct row indices in [0, n), returned sorted ascending."""
+    S = np.asarray(rows, dtype=np.int64).reshape(-1)
+    if S.size != k or np.unique(S).size != k or (k and (S.min() < 0 or S.max() >= n)):
+        raise ValueError("rows must be k distinct indices in [0, n)")
+    return np.sort(S)
+
+
 def dion3_step(W, M, G, f_num: int, f_den: int, mu: float, eta: float, wd: float = 0.0,
-               norm_p: int = 1, abc=None, restart_after=(), eps: float = 1e-7):
+               norm_p: int = 1, abc=None, restart_after=(), eps: float = 1e-7, rows=None):
     """One Dion3 step on one n x m matrix (n <= m).
 
+    ``rows``: optional caller-chosen S (k distinct indices); then no keys are computed.
     Returns (W_new float64, M_new fp32, S int64 ascending, O float64 k x m).
     """
     M = np.asarray(M, dtype=np.float32)
@@ -90,9 +104,11 @@ def dion3_step(W, M, G, f_num: int, f_den: int, mu: float, eta: float, wd: float
     if n > m:
         raise ValueError("orient the matrix so that n <= m")
     M1 = (M.astype(np.float64) + np.asarray(G, dtype=np.float64)).astype(np.float32)
-    keys = exact_row_keys(M1, norm_p)
     k = ceil_k(n, f_num, f_den)
-    S = top_k_rows(keys, k)
+    if rows is None:
+        S = top_k_rows(exact_row_keys(M1, norm_p), k)
+    else:
+        S = given_rows(rows, n, k)
     O = gram_ns(M1[S].astype(np.float64), abc, restart_after, eps)
     eta_p = eta * math.sqrt(f_den / f_num)
     W1 = np.asarray(W, dtype=np.float64) * (1.0 - eta_p * wd)

@@ -164,3 +164,44 @@ def test_weight_decay_uses_eta_prime(jordan):
     sel = np.zeros(n, bool)
     sel[S] = True
     np.testing.assert_allclose(W1[~sel], W[~sel].astype(np.float64) * (1 - 0.02 * wd), rtol=0, atol=0)
+
+
+@pytest.mark.parametrize("f", [(1, 4), (3, 8)])
+def test_given_rows_follow_error_feedback(f, jordan):
+    """A caller-chosen S ('limitations': random selection): M[S] = fl32(mu (M+G)), the other rows
+    are M+G bit for bit, W changes only on S, and the update on S is eta' times the polar factor
+    of M[S] (checked against an SVD with the classic cubic run to convergence)."""
+    n, m = 20, 48
+    W, M, G = _step_inputs(n, m, seed=11)
+    k = oracle.ceil_k(n, *f)
+    rows = np.random.default_rng(5).choice(n, size=k, replace=False)
+    mu, eta = 0.9, 0.01
+    cubic = [(1.5, -0.5, 0.0)] * 60
+    W1, M1, S, O = oracle.dion3_step(W, M, G, *f, mu=mu, eta=eta, abc=cubic, rows=rows)
+    assert list(S) == sorted(rows.tolist())
+    summed = M + G
+    sel = np.zeros(n, bool)
+    sel[S] = True
+    assert np.array_equal(M1[~sel].view(np.uint32), summed[~sel].view(np.uint32))
+    assert np.array_equal(M1[sel].view(np.uint32), (np.float32(mu) * summed)[sel].view(np.uint32))
+    assert np.array_equal(W1[~sel], W[~sel].astype(np.float64))
+    U, _, Vt = np.linalg.svd(summed[S].astype(np.float64), full_matrices=False)
+    eta_p = eta * math.sqrt(f[1] / f[0])
+    np.testing.assert_allclose(W1[S] - W[S].astype(np.float64), -eta_p * (U @ Vt), rtol=0, atol=1e-10)
+
+
+def test_given_rows_equal_to_topk_reproduce_default(jordan):
+    n, m = 24, 40
+    W, M, G = _step_inputs(n, m, seed=12)
+    a = oracle.dion3_step(W, M, G, 1, 4, mu=0.95, eta=0.01, abc=[jordan] * 5, restart_after=(2,))
+    b = oracle.dion3_step(W, M, G, 1, 4, mu=0.95, eta=0.01, abc=[jordan] * 5, restart_after=(2,),
+                          rows=a[2][::-1].copy())
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("rows", [[0, 0, 1, 2, 3, 4], [0, 1, 2, 3, 4, 24], [0, 1, 2], [-1, 1, 2, 3, 4, 5]])
+def test_given_rows_validated(rows, jordan):
+    W, M, G = _step_inputs(24, 40, seed=13)
+    with pytest.raises(ValueError):
+        oracle.dion3_step(W, M, G, 1, 4, mu=0.95, eta=0.01, abc=[jordan] * 5, rows=rows)
