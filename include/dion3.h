@@ -56,10 +56,14 @@ typedef enum {
 /* Element types. */
 typedef enum { DION3_BF16 = 0, DION3_FP16 = 1, DION3_FP32 = 2 } dion3_dtype;
 
+/* norm_p value of the step entry points for a caller-chosen row set S (see dion3_step). */
+#define DION3_SELECT_GIVEN 0
+
 /* Bits OR-ed into *status_dev by kernels. */
 #define DION3_DEV_NONFINITE 0x1 /* a non-finite momentum key, norm or input value was seen */
 #define DION3_DEV_TIMEOUT   0x2 /* a bounded wait gave up; outputs of that call are undefined */
-#define DION3_DEV_SELECT    0x4 /* row selection could not certify k rows (internal error) */
+#define DION3_DEV_SELECT    0x4 /* row selection could not certify k rows (internal error), or a
+                                   caller-chosen S was not k distinct ascending rows in [0, n) */
 
 /*
  * dion3_sym_gemm -- D = alpha * A * B^T + beta * C + gamma * I, for results known to be
@@ -197,6 +201,12 @@ size_t dion3_step_workspace_bytes(int batch, int n, int m, int f_num, int f_den,
  *       written ascending to sel_out.  Keys are compared as exact real numbers: fp32 keys
  *       with a proven error bound decide every row they can, and the rows they cannot are
  *       re-ranked with exact integer sums on the device.
+ *   norm_p = DION3_SELECT_GIVEN: S is chosen by the caller and read from sel_out (k strictly
+ *       ascending rows in [0, n) per matrix; e.g. a random subset, which [D3] "limitations"
+ *       reports to work about as well, and which [D3] "future directions" notes can be drawn
+ *       without knowing M).  No keys are computed.  A matrix whose S breaks the rule gets
+ *       DION3_DEV_SELECT, its sel_out entries are set to -1 and none of its rows change
+ *       except by M <- M + G (and the decay of W).
  *   O = GramNS(M[S,:])                          (as dion3_gram_ns, compute_dtype)
  *   W <- (1 - eta' wd) W  (all rows; skipped when wd == 0)
  *   W[S,:] <- W[S,:] - eta' O,  eta' = eta * sqrt(f_den / f_num)

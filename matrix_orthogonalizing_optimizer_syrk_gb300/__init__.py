@@ -64,6 +64,8 @@ SIGNATURES = {
     "dion3_selftest_watchdog": (_c_int, [ctypes.c_longlong, _c_p, _c_p]),
 }
 
+SELECT_GIVEN = 0  # norm_p of a caller-chosen row set (DION3_SELECT_GIVEN)
+
 _lib = None
 
 
@@ -260,7 +262,7 @@ def step(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, f=(1, 4), mu: float 
          wd: float = 0.0, norm_p: int = 1, abc=None, restart_after=(2,), eps: float = 1e-7, compute=torch.float16,
          sel_out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
          status: torch.Tensor | None = None, events=None, hyper: torch.Tensor | None = None,
-         decay: bool = False) -> torch.Tensor:
+         decay: bool = False, rows: torch.Tensor | None = None) -> torch.Tensor:
     """One Dion3 step on [batch, n, m] (or [n, m]) contiguous W, M (fp32) and G; returns the selected rows.
 
     ``events``: optional list of up to five recorded-once ``torch.cuda.Event`` objects, recorded
@@ -268,6 +270,9 @@ def step(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, f=(1, 4), mu: float 
     ``hyper``: optional fp32 device tensor {mu, eta, wd}; the kernels read it when they run
     (``mu``, ``eta``, ``wd`` are then ignored and ``decay`` turns the W decay pass on), so the
     call can be captured in a CUDA graph once and replayed with new values.
+    ``rows``: optional caller-chosen row set S, int32 [batch, k] (or [k]) with strictly ascending
+    rows per matrix (e.g. a sorted random subset); no keys are computed (``norm_p`` is ignored).
+    A matrix whose rows break the rule is left unselected and flags DION3_DEV_SELECT.
     """
     for t, name in ((W, "W"), (M, "M"), (G, "G")):
         _cuda(t, name)
@@ -282,9 +287,16 @@ def step(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, f=(1, 4), mu: float 
     k = k_of(n, f_num, f_den)
     if k < 0:
         raise ValueError("need 0 < f <= 1")
+    shape = (k,) if M.dim() == 2 else (batch, k)
     if sel_out is None:
-        shape = (k,) if M.dim() == 2 else (batch, k)
         sel_out = torch.empty(shape, dtype=torch.int32, device=M.device)
+    if rows is not None:
+        _cuda(rows, "rows")
+        if rows.dtype != torch.int32 or tuple(rows.shape) != shape:
+            raise ValueError(f"rows must be int32 of shape {shape}")
+        if rows.data_ptr() != sel_out.data_ptr():
+            sel_out.copy_(rows)
+        norm_p = SELECT_GIVEN
     T, flat, rarr, nr = _abc_arrays(abc, restart_after)
     need = workspace_bytes_step(batch, n, m, f_num, f_den, norm_p, compute, nr)
     if workspace is None:

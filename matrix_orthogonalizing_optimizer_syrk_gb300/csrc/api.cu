@@ -489,7 +489,7 @@ int dion3_ns_standard(int batch, int n, int m, const void* X, int64_t ldx, int64
 size_t dion3_step_workspace_bytes(int batch, int n, int m, int f_num, int f_den, int norm_p, int compute_dtype,
                                   int n_restart) {
   if (batch < 0 || n < 0 || m < n || n_restart < 0) return 0;
-  if (norm_p != 1 && norm_p != 2) return 0;
+  if (norm_p != DION3_SELECT_GIVEN && norm_p != 1 && norm_p != 2) return 0;
   if (!dtype_valid(compute_dtype)) return 0;
   const int k = dion3_k(n, f_num, f_den);
   if (k < 0) return 0;
@@ -524,7 +524,7 @@ int step_impl(int batch, int n, int m, float* W, float* M, const void* G, int g_
   if (n_events < 0 || (n_events > 0 && events == nullptr)) return DION3_EINVAL;
   if (batch < 0 || n < 0 || m < 0) return DION3_EINVAL;
   if (!dtype_valid(g_dtype) || !dtype_valid(compute_dtype)) return DION3_EINVAL;
-  if (norm_p != 1 && norm_p != 2) return DION3_EINVAL;
+  if (norm_p != DION3_SELECT_GIVEN && norm_p != 1 && norm_p != 2) return DION3_EINVAL;
   const int k = dion3_k(n, f_num, f_den);
   if (k < 0) return DION3_EINVAL;
   if (int rc = check_schedule(T, abc, restart_after, n_restart)) return rc;

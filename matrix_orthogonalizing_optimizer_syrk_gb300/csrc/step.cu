@@ -11,6 +11,8 @@
 //           2^-149, every square one of 2^-298).
 //           Pass A also stores each row's sum of squares; pass B adds them up over S for the
 //           Frobenius prescale, scale_b = 1 / (||M[S,:]||_F + eps).
+//           With a caller-chosen S (norm_p = DION3_SELECT_GIVEN: the pages' random selection)
+//           pass A computes no keys and pass B only checks S (k distinct ascending rows).
 //   pass C  X_S = scale_b * M[S,:] packed in the compute dtype, and M[S,:] <- mu * M[S,:]
 //           (fp32, one rounding).
 // The W row update W[S,:] -= eta' O is fused into the last GEMM's epilogue (gemm_tc.cu).
@@ -432,6 +434,25 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const BArgs a) {
   selected_scale(a, b, sel);
 }
 
+// Pass B for a caller-chosen S: sel[b] must hold k strictly ascending rows in [0, n).  A set
+// that breaks this is flagged (DION3_DEV_SELECT) and replaced by -1 entries, so that no row
+// of W or M is touched for that matrix.
+__global__ void __launch_bounds__(256) given_kernel(const BArgs a) {
+  const int b = blockIdx.x;
+  int32_t* sel = a.sel + static_cast<long long>(b) * a.k;
+  int bad = 0;
+  for (int j = threadIdx.x; j < a.k; j += blockDim.x) {
+    const int i = sel[j];
+    bad |= i < 0 || i >= a.n || (j > 0 && sel[j - 1] >= i);
+  }
+  if (__syncthreads_or(bad)) {
+    for (int j = threadIdx.x; j < a.k; j += blockDim.x) sel[j] = -1;
+    if (threadIdx.x == 0 && a.status) atomicOr(a.status, DION3_DEV_SELECT);
+  }
+  __syncthreads();
+  selected_scale(a, b, sel);
+}
+
 // ------------------------------------------------------------------------------ pass C
 struct CArgs {
   int n, m, k;
@@ -506,7 +527,7 @@ int launch_a(const AArgs& a, bool vec, cudaStream_t s) {
 
 template <typename TG>
 int launch_a_p(const AArgs& a, int norm_p, bool vec, cudaStream_t s) {
-  return norm_p == 1 ? launch_a<TG, 1>(a, vec, s) : launch_a<TG, 2>(a, vec, s);
+  return norm_p == 2 ? launch_a<TG, 2>(a, vec, s) : launch_a<TG, 1>(a, vec, s);  // no keys: a.keys is off
 }
 
 template <typename TC>
@@ -526,7 +547,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
-int step_exact_limbs(int norm_p) { return norm_p == 1 ? 5 : 9; }
+int step_exact_limbs(int norm_p) { return norm_p == 1 ? 5 : (norm_p == 2 ? 9 : 0); }
 
 int step_momentum_keys(const StepArgs& s, cudaStream_t st) {
   AArgs a{};
@@ -539,7 +560,7 @@ int step_momentum_keys(const StepArgs& s, cudaStream_t st) {
   a.decay = s.decay;
   a.hyper = s.hyper;
   a.eta_scale = s.eta_scale;
-  a.keys = s.k < s.n;
+  a.keys = s.norm_p != DION3_SELECT_GIVEN && s.k < s.n;
   a.key_lo = s.key_lo;
   a.key_hi = s.key_hi;
   a.rowsq = s.rowsq;
@@ -572,6 +593,11 @@ int step_select(const StepArgs& s, cudaStream_t st) {
   a.scale = s.scale;
   a.eps = s.eps;
   a.status = s.status;
+  if (s.norm_p == DION3_SELECT_GIVEN) {
+    if (s.k <= 0) return DION3_OK;
+    given_kernel<<<s.batch, 256, 0, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? DION3_OK : DION3_ECUDA;
+  }
   const int smem = 11 * s.n + 16;
   if (s.norm_p == 1) {
     if (cudaFuncSetAttribute(select_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)

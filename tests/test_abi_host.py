@@ -200,3 +200,11 @@ def test_step_dev_validation(L):
     assert call(W=NULL) == 1
     assert call(ws=NULL) == 3
     assert call(n=0) == 0
+
+
+def test_given_selection_mode_accepted(L):
+    """norm_p = DION3_SELECT_GIVEN passes validation (nothing launched: workspace too small)."""
+    assert _step(L, p=0, wsb=16) == 3
+    assert _step(L, p=3) == 1
+    assert d3.workspace_bytes_step(2, 64, 128, 1, 4, 0, 0, 2) > 0
+    assert d3.workspace_bytes_step(2, 64, 128, 1, 4, 0, 0, 2) < d3.workspace_bytes_step(2, 64, 128, 1, 4, 1, 0, 2)

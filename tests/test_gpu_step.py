@@ -148,3 +148,73 @@ def test_megabatch_full_size_two_steps(shape, count, f):
             synthetic.lowrank_plus_noise(n, m, 4000 + i + 10 ** 6 * step, dtype=torch.bfloat16, device=DEV, out=G[i])
         _run_and_check(W, M, G, f, 0.95, 0.01, 1, (2, 4), idx=idx)
         del G
+
+
+def _random_rows(batch, n, k, seed):
+    rng = np.random.default_rng(seed)
+    return np.stack([np.sort(rng.choice(n, size=k, replace=False)) for _ in range(batch)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("n,m,f", [(64, 256, (1, 4)), (130, 1000, (1, 8)), (96, 1004, (3, 5))])
+def test_given_random_rows(n, m, f):
+    """A caller-chosen S (random selection): the same rows are used, M bit-exact, Delta W in 3e-2."""
+    batch = 3
+    k = d3.k_of(n, *f)
+    W = synthetic.gaussian((batch, n, m), seed=13, std=0.02, device=DEV)
+    M = synthetic.gaussian((batch, n, m), seed=14, std=0.01, device=DEV)
+    G = synthetic.lowrank_batch(batch, n, m, base_seed=500 + n, dtype=torch.bfloat16, device=DEV)
+    rows = _random_rows(batch, n, k, seed=n)
+    W0, M0, Gc = W.cpu().numpy().copy(), M.cpu().numpy().copy(), G.float().cpu().numpy()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sel = d3.step(W, M, G, f=f, mu=0.9, eta=0.01, abc=ABC, restart_after=(2, 4),
+                  rows=torch.from_numpy(rows).to(DEV), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(sel.cpu().numpy(), rows)
+    for i in range(batch):
+        W1, M1, S, _ = oracle.dion3_step(W0[i], M0[i], Gc[i], *f, mu=0.9, eta=0.01, abc=ABC, restart_after=(2, 4),
+                                         rows=rows[i])
+        assert np.array_equal(bits32(M[i]), bits32(M1))
+        dW = W[i].double().cpu().numpy() - W0[i]
+        assert rel_frob(dW, W1 - W0[i]) <= 3e-2
+
+
+def test_given_rows_equal_to_topk_match_default_bitwise():
+    n, m = 128, 512
+    W = synthetic.gaussian((2, n, m), seed=15, std=0.02, device=DEV)
+    M = synthetic.gaussian((2, n, m), seed=16, std=0.01, device=DEV)
+    G = synthetic.lowrank_batch(2, n, m, base_seed=520, dtype=torch.bfloat16, device=DEV)
+    Wa, Ma = W.clone(), M.clone()
+    sel = d3.step(Wa, Ma, G, f=(1, 4), abc=ABC, restart_after=(2,))
+    Wb, Mb = W.clone(), M.clone()
+    sel_b = d3.step(Wb, Mb, G, f=(1, 4), abc=ABC, restart_after=(2,), rows=sel.clone())
+    torch.cuda.synchronize()
+    assert torch.equal(sel, sel_b)
+    assert torch.equal(Ma, Mb) and torch.equal(Wa, Wb)
+
+
+def test_invalid_given_rows_leave_that_matrix_unselected():
+    """Matrix 1 gets a repeated row, matrix 2 an out-of-range one: both are flagged and left
+    alone (W unchanged, M only + G); matrix 0 is stepped normally."""
+    n, m, f = 64, 256, (1, 4)
+    k = d3.k_of(n, *f)
+    W = synthetic.gaussian((3, n, m), seed=17, std=0.02, device=DEV)
+    M = synthetic.gaussian((3, n, m), seed=18, std=0.01, device=DEV)
+    G = synthetic.lowrank_batch(3, n, m, base_seed=540, dtype=torch.bfloat16, device=DEV)
+    rows = _random_rows(3, n, k, seed=3)
+    rows[1, 1] = rows[1, 0]
+    rows[2, -1] = n
+    W0, M0, Gc = W.cpu().numpy().copy(), M.cpu().numpy().copy(), G.float().cpu().numpy()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sel = d3.step(W, M, G, f=f, mu=0.9, eta=0.01, abc=ABC, restart_after=(2,),
+                  rows=torch.from_numpy(rows).to(DEV), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 0x4
+    assert (sel[1:] == -1).all()
+    for i in (1, 2):
+        assert np.array_equal(W[i].cpu().numpy(), W0[i])
+        assert np.array_equal(bits32(M[i]), bits32(M0[i] + Gc[i].astype(np.float32)))
+    W1, M1, S, _ = oracle.dion3_step(W0[0], M0[0], Gc[0], *f, mu=0.9, eta=0.01, abc=ABC, restart_after=(2,),
+                                     rows=rows[0])
+    assert np.array_equal(bits32(M[0]), bits32(M1))
+    assert rel_frob(W[0].double().cpu().numpy() - W0[0], W1 - W0[0]) <= 3e-2
