@@ -32,22 +32,30 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int NUM_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int EPI_WARPS = 4;
+// Warp 0 issues TMA loads, warp 1 the MMAs, the remaining warps drain the accumulators: four
+// for the stored products, eight for the W row update, whose epilogue streams W through
+// registers and needs the extra warps to keep enough loads in flight.
+template <int EPI>
+constexpr int epi_warps() { return EPI == EPI_WUPD ? 8 : 4; }
+template <int EPI>
+constexpr int num_threads() { return 64 + 32 * epi_warps<EPI>(); }
 constexpr long long DEFAULT_SPIN = 4000000000LL;  // clock cycles (about 2 s)
 
 // CL = 1: one CTA computes a 128 x BN tile.  CL = 2: a CTA pair computes a 256 x BN tile with
 // tcgen05.mma.cta_group::2 -- each CTA holds its 128 rows of A and half (BN / 2) of B, so
 // every SM stages and reads only half of the B tile.
-template <int BN, int CL>
+template <int BN, int CL, int EPI>
 struct Cfg {
+  static constexpr int EPIW = epi_warps<EPI>();
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = (BN / CL) * BK * 2;
-  static constexpr int STAGES = (196608 / (A_BYTES + B_BYTES)) < 8 ? (196608 / (A_BYTES + B_BYTES)) : 8;
-  // Epilogue staging: per epilogue warp, two buffers of {32x32 block, its transpose} in 16 bits.
+  // Epilogue staging per warp: two buffers of {32x32 block, its transpose} in 16 bits (stored
+  // products), or one 32 x 36 fp32 block and 32 row pointers (W row update).
+  static constexpr int STG_WARP = EPI == EPI_WUPD ? 5120 : 2 * 2 * 2048;
+  static constexpr int STAGE_BUDGET = 232448 - EPIW * STG_WARP - 2048;  // 227 KB minus staging and barriers
+  static constexpr int STAGES = (STAGE_BUDGET / (A_BYTES + B_BYTES)) < 8 ? (STAGE_BUDGET / (A_BYTES + B_BYTES)) : 8;
   static constexpr int STG_OFF = STAGES * (A_BYTES + B_BYTES);
-  static constexpr int STG_WARP = 2 * 2 * 2048;
-  static constexpr int BAR_OFF = STG_OFF + EPI_WARPS * STG_WARP;
+  static constexpr int BAR_OFF = STG_OFF + EPIW * STG_WARP;
   static constexpr int NBARS = 2 * STAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain
   static constexpr int SMEM = BAR_OFF + NBARS * 8 + 16 + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -434,55 +442,86 @@ __device__ __forceinline__ void epi_tile_tma(const KParams& p, const CUtensorMap
   }
 }
 
-// 32 fp32 values of W starting at column c0 of `wrow` (zeros outside the matrix).
-__device__ __forceinline__ void load_w32(const float* wrow, int c0, int N, float4 (&x)[8]) {
-  if (wrow != nullptr && c0 + 31 < N && aligned16(wrow + c0)) {
-    const float4* s4 = reinterpret_cast<const float4*>(wrow + c0);
+// Epilogue of the fused row update W[sel[r], :] += alpha * acc.  tcgen05.ld hands each lane one
+// accumulator row; addressed that way, every warp access to W would touch 32 scattered rows.
+// So each 32 x 32 chunk goes through shared memory and is read back transposed: in the global
+// loads and stores, lanes 8j .. 8j+7 cover 128 contiguous bytes of one W row and a warp
+// instruction covers four rows.  NHALF warps share a lane quarter and take every NHALF-th
+// chunk; each runs its W loads AHEAD chunks in front of the adds and stores.  Staging per warp:
+// the 32 x 36 fp32 chunk and 32 row pointers (4864 bytes).
+template <bool CHECKED>
+__device__ __forceinline__ void load_w_chunk(float* const (&wr)[8], int c, int N, float4 (&x)[8]) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = s4[i];
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int c = c0 + 4 * i;
-      x[i].x = (wrow && c < N) ? wrow[c] : 0.f;
-      x[i].y = (wrow && c + 1 < N) ? wrow[c + 1] : 0.f;
-      x[i].z = (wrow && c + 2 < N) ? wrow[c + 2] : 0.f;
-      x[i].w = (wrow && c + 3 < N) ? wrow[c + 3] : 0.f;
+  for (int it = 0; it < 8; ++it) {
+    const float* w = wr[it];
+    if (!CHECKED) {
+      x[it] = *reinterpret_cast<const float4*>(w + c);
+    } else {
+      x[it].x = (w && c < N) ? w[c] : 0.f;
+      x[it].y = (w && c + 1 < N) ? w[c + 1] : 0.f;
+      x[it].z = (w && c + 2 < N) ? w[c + 2] : 0.f;
+      x[it].w = (w && c + 3 < N) ? w[c + 3] : 0.f;
     }
   }
 }
 
-// Epilogue of the fused row update W[sel[r], :] += alpha * acc.  Each lane streams 32 fp32
-// values (128 bytes) of its W row per chunk; with the chunk loop unrolled, the loads run three
-// chunks ahead of the adds and stores (about 3 x 4 KB in flight per warp), enough to cover
-// DRAM latency for these scattered rows.
-template <int BN>
-__device__ __forceinline__ void epi_tile_wupd(const KParams& p, uint32_t t_acc, int b, int mi, int nj, int ew,
-                                              int lane, float ab) {
-  constexpr int NCH = BN / 32;
-  constexpr int AHEAD = 3;
+template <int BN, int NHALF>
+__device__ __forceinline__ void epi_tile_wupd(const KParams& p, uint8_t* stg, uint32_t t_acc, int b, int mi, int nj,
+                                              int ew, int half, int lane, float ab) {
+  constexpr int NCHW = BN / 32 / NHALF;  // chunks of this warp
+  constexpr int AHEAD = NHALF == 1 ? 3 : 2;
+  constexpr int LDT = 36;  // staged row stride in floats (16-byte aligned, conflict-free phases)
   const int r0w = mi * BM + ew * 32;
   if (r0w >= p.M) return;
-  const int r = r0w + lane;
-  float* wrow = nullptr;
-  if (r < p.M) {
-    const int row = __ldg(p.sel + static_cast<long long>(b) * p.ssel + r);
-    if (row >= 0 && row < p.w_rows)  // only a failed selection leaves rows outside [0, w_rows)
-      wrow = p.W + static_cast<long long>(b) * p.sW + static_cast<long long>(row) * p.ldw;
+  float* tile = reinterpret_cast<float*>(stg);
+  float** rowp = reinterpret_cast<float**>(stg + 32 * LDT * 4);
+  {
+    const int r = r0w + lane;
+    float* wrow = nullptr;
+    if (r < p.M) {
+      const int row = __ldg(p.sel + static_cast<long long>(b) * p.ssel + r);
+      if (row >= 0 && row < p.w_rows)  // only a failed selection leaves rows outside [0, w_rows)
+        wrow = p.W + static_cast<long long>(b) * p.sW + static_cast<long long>(row) * p.ldw;
+    }
+    __syncwarp();
+    rowp[lane] = wrow;
+    __syncwarp();
   }
+  const int sub = lane >> 3;      // row within each group of four
+  const int cq = (lane & 7) * 4;  // first of this lane's four columns in a chunk
+  float* wr[8];
+  bool rows_ok = true;
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    wr[it] = rowp[it * 4 + sub];
+    rows_ok &= wr[it] != nullptr;
+  }
+  // Fast path: 16-byte aligned W rows, all 32 rows present; then only the chunk's columns matter.
+  const bool fast = __all_sync(0xffffffffu, rows_ok) && ((p.ldw & 3) == 0) && ((p.sW & 3) == 0) && aligned16(p.W);
   float4 ring[AHEAD][8];
 #pragma unroll
-  for (int ch = 0; ch < AHEAD && ch < NCH; ++ch) {
-    if (nj * BN + ch * 32 < p.N) load_w32(wrow, nj * BN + ch * 32, p.N, ring[ch]);
+  for (int j = 0; j < AHEAD && j < NCHW; ++j) {
+    const int c0 = nj * BN + (half + j * NHALF) * 32;
+    if (c0 < p.N) {
+      if (fast && c0 + 32 <= p.N) load_w_chunk<false>(wr, c0 + cq, p.N, ring[j]);
+      else load_w_chunk<true>(wr, c0 + cq, p.N, ring[j]);
+    }
   }
 #pragma unroll
-  for (int ch = 0; ch < NCH; ++ch) {
+  for (int j = 0; j < NCHW; ++j) {
+    const int ch = half + j * NHALF;
     const int c0 = nj * BN + ch * 32;
     if (c0 < p.N) {
       float4 x[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = ring[ch % AHEAD][i];
-      if (ch + AHEAD < NCH && c0 + AHEAD * 32 < p.N) load_w32(wrow, c0 + AHEAD * 32, p.N, ring[ch % AHEAD]);
+      for (int i = 0; i < 8; ++i) x[i] = ring[j % AHEAD][i];
+      if (j + AHEAD < NCHW) {
+        const int cn = c0 + AHEAD * NHALF * 32;
+        if (cn < p.N) {
+          if (fast && cn + 32 <= p.N) load_w_chunk<false>(wr, cn + cq, p.N, ring[j % AHEAD]);
+          else load_w_chunk<true>(wr, cn + cq, p.N, ring[j % AHEAD]);
+        }
+      }
       uint32_t v[32];
       __syncwarp();
       if (p.num_kb > 0) {
@@ -491,31 +530,33 @@ __device__ __forceinline__ void epi_tile_wupd(const KParams& p, uint32_t t_acc, 
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0u;
       }
-      if (wrow != nullptr) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          x[i].x = fmaf(__uint_as_float(v[4 * i + 0]), ab, x[i].x);
-          x[i].y = fmaf(__uint_as_float(v[4 * i + 1]), ab, x[i].y);
-          x[i].z = fmaf(__uint_as_float(v[4 * i + 2]), ab, x[i].z);
-          x[i].w = fmaf(__uint_as_float(v[4 * i + 3]), ab, x[i].w);
-        }
-        if (c0 + 31 < p.N && aligned16(wrow + c0)) {
-          float4* d4 = reinterpret_cast<float4*>(wrow + c0);
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4*>(tile + lane * LDT + 4 * q) = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      __syncwarp();
+      const int c = c0 + cq;
+      const bool full_chunk = fast && c0 + 32 <= p.N;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) d4[i] = x[i];
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int c = c0 + 4 * i;
-            if (c < p.N) wrow[c] = x[i].x;
-            if (c + 1 < p.N) wrow[c + 1] = x[i].y;
-            if (c + 2 < p.N) wrow[c + 2] = x[i].z;
-            if (c + 3 < p.N) wrow[c + 3] = x[i].w;
-          }
+      for (int it = 0; it < 8; ++it) {
+        const float4 a = *reinterpret_cast<const float4*>(tile + (it * 4 + sub) * LDT + cq);
+        float4 y = x[it];
+        y.x = fmaf(a.x, ab, y.x);
+        y.y = fmaf(a.y, ab, y.y);
+        y.z = fmaf(a.z, ab, y.z);
+        y.w = fmaf(a.w, ab, y.w);
+        float* w = wr[it];
+        if (full_chunk) {
+          *reinterpret_cast<float4*>(w + c) = y;
+        } else if (w != nullptr) {
+          if (c < p.N) w[c] = y.x;
+          if (c + 1 < p.N) w[c + 1] = y.y;
+          if (c + 2 < p.N) w[c + 2] = y.z;
+          if (c + 3 < p.N) w[c + 3] = y.w;
         }
       }
     }
   }
+  __syncwarp();
 }
 
 // Wait that ignores the abort flag (used while draining after an abort), bounded by time.
@@ -528,10 +569,10 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long l
 
 // ----------------------------------------------------------------------------- kernel
 template <int BN, bool B_MN, int EPI, int CL>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(num_threads<EPI>(), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const KParams p) {
-  using Cf = Cfg<BN, CL>;
+  using Cf = Cfg<BN, CL, EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -558,7 +599,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(tfull0 + 8 * a, 1);
-      ptx::mbar_init(tempty0 + 8 * a, EPI_WARPS * CL);  // every epilogue warp of the pair releases it
+      ptx::mbar_init(tempty0 + 8 * a, Cf::EPIW * CL);  // every epilogue warp of the pair releases it
     }
     ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -701,7 +742,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ------------------------------------------------ epilogue (warps 2..5)
     const int ew = warp & 3;  // TMEM lanes 32*ew .. 32*ew+31
-    uint8_t* stg = smem + Cf::STG_OFF + ew * Cf::STG_WARP;
+    const int half = (warp - 2) >> 2;  // W row update: the two warps of a lane quarter split the chunks
+    uint8_t* stg = smem + Cf::STG_OFF + (warp - 2) * Cf::STG_WARP;
     int buf = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -718,7 +760,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(acc * BN);
       bool done = false;
       if constexpr (EPI == EPI_WUPD) {
-        epi_tile_wupd<BN>(p, t_acc, b, mi, nj, ew, lane, ab);
+        epi_tile_wupd<BN, Cf::EPIW / 4>(p, stg, t_acc, b, mi, nj, ew, half, lane, ab);
         done = true;
       } else {
         if (p.d_type != FP32) {
@@ -849,8 +891,8 @@ int max_clusters() {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<BN, 2>::SMEM;
+  cfg.blockDim = dim3(num_threads<EPI>(), 1, 1);
+  cfg.dynamicSmemBytes = Cfg<BN, 2, EPI>::SMEM;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
@@ -864,7 +906,7 @@ int max_clusters() {
 
 template <int BN, bool B_MN, int EPI, int CL>
 int launch(const GemmCall& g, cudaStream_t s) {
-  using Cf = Cfg<BN, CL>;
+  using Cf = Cfg<BN, CL, EPI>;
   KParams p{};
   p.batch = g.batch;
   p.M = g.M;
@@ -936,7 +978,7 @@ int launch(const GemmCall& g, cudaStream_t s) {
   if constexpr (CL == 1) {
     long long grid = sm_count();
     if (grid > p.total_tiles) grid = p.total_tiles;
-    kern<<<static_cast<unsigned>(grid), NUM_THREADS, Cf::SMEM, s>>>(ta, tb, td, p);
+    kern<<<static_cast<unsigned>(grid), num_threads<EPI>(), Cf::SMEM, s>>>(ta, tb, td, p);
   } else {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -944,7 +986,7 @@ int launch(const GemmCall& g, cudaStream_t s) {
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.blockDim = dim3(num_threads<EPI>(), 1, 1);
     cfg.dynamicSmemBytes = Cf::SMEM;
     cfg.stream = s;
     cfg.attrs = attr;
