@@ -1020,8 +1020,14 @@ int gemm_tc(const GemmCall& g, cudaStream_t s) {
   // Pairs of 128-row blocks share each 256-column B tile through cluster multicast when there
   // are at least two row blocks; otherwise one CTA per tile.
   switch (g.epi) {
-    case EPI_SYM:
-      return g.M <= 128 ? launch<128, false, EPI_SYM, 1>(g, s) : launch<256, false, EPI_SYM, 2>(g, s);
+    case EPI_SYM: {
+      // CTA pairs on 256 x 256 tiles, unless that leaves SMs idle: then 128 x 128 tiles, which
+      // give about twice as many CTAs (small single products such as n <= 2048).
+      const long long pairs = (g.M + 255) / 256;
+      const long long pair_ctas = 2 * pairs * (pairs + 1) / 2 * g.batch;
+      if (g.M <= 128 || pair_ctas < sm_count()) return launch<128, false, EPI_SYM, 1>(g, s);
+      return launch<256, false, EPI_SYM, 2>(g, s);
+    }
     case EPI_GEN:
       if (g.N <= 128) return launch<128, true, EPI_GEN, 1>(g, s);
       return g.M <= 128 ? launch<256, true, EPI_GEN, 1>(g, s) : launch<256, true, EPI_GEN, 2>(g, s);
