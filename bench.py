@@ -427,8 +427,18 @@ def bench_gram_ns(torch, d3, synthetic, dev, peaks, peaks_kind):
         torch.cuda.synchronize()
         ms = _time_calls(torch, fn, 3)
         fl = float(B * gram_flops(n, m))
-        out["batches"].append({"shape": f"{B}x{n}x{m}", "ms": ms, "matrices_per_s": B / ms * 1e3,
-                               "TFLOP/s": fl / ms / 1e9})
+        entry = {"shape": f"{B}x{n}x{m}", "ms": ms, "matrices_per_s": B / ms * 1e3, "TFLOP/s": fl / ms / 1e9}
+        if n == m:
+            # alpha = 1: the standard Newton-Schulz fallback on the same batch (T (3 alpha + 1) n^3 FLOPs)
+            ws2 = torch.empty(d3.workspace_bytes_ns_standard(B, n, m, torch.float16), dtype=torch.uint8, device=dev)
+            fn2 = lambda: d3.ns_standard(X, ABC, compute=torch.float16, out=O, workspace=ws2)  # noqa: E731
+            fn2()
+            torch.cuda.synchronize()
+            ms2 = _time_calls(torch, fn2, 3)
+            fl2 = float(B * T_ITERS * (3 * m / n + 1) * n ** 3)
+            entry["ns_standard_fallback"] = {"ms": ms2, "matrices_per_s": B / ms2 * 1e3, "TFLOP/s": fl2 / ms2 / 1e9}
+            del ws2
+        out["batches"].append(entry)
         total_ms += ms
         total_flops += fl
         del X, O, ws
@@ -495,8 +505,15 @@ def bench_gram_fp32(torch, d3, synthetic, dev):
     fn()
     torch.cuda.synchronize()
     ms = _time_calls(torch, fn, 20)
+    # the same call captured once in a CUDA graph and replayed (no per-launch host work)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fn()
+    graph.replay()
+    torch.cuda.synchronize()
+    ms_g = _time_calls(torch, graph.replay, 20)
     return {"workload": "gram_ns fp32 (FFMA) 256x1024, T=5 Jordan, restart after 2", "us": ms * 1e3,
-            "matrices_per_s": 1e3 / ms}
+            "matrices_per_s": 1e3 / ms, "cuda_graph_us": ms_g * 1e3}
 
 
 def bench_sym_gemm(torch, d3, synthetic, dev, peaks, peaks_kind):
