@@ -492,17 +492,27 @@ __global__ void __launch_bounds__(256) gather_kernel(const CArgs a) {
     float* src = a.M + (b * a.n + i) * a.m;
     const float f = a.scale[b];
     if constexpr (VEC) {
-      for (int c = lane * 4; c < a.m; c += 128) {
-        float4* s4 = reinterpret_cast<float4*>(src + c);
-        const float4 x = *s4;
+      // Four 16-byte loads per lane are issued before any store, so each warp keeps 2 KB of the
+      // row in flight.
+      auto put = [&](int c, const float4& x) {
         if constexpr (sizeof(TC) == 2) {
           TC o[4] = {cvt_out<TC>(x.x * f), cvt_out<TC>(x.y * f), cvt_out<TC>(x.z * f), cvt_out<TC>(x.w * f)};
           *reinterpret_cast<uint2*>(dst + c) = *reinterpret_cast<const uint2*>(o);
         } else {
           *reinterpret_cast<float4*>(dst + c) = make_float4(x.x * f, x.y * f, x.z * f, x.w * f);
         }
-        *s4 = make_float4(__fmul_rn(mu, x.x), __fmul_rn(mu, x.y), __fmul_rn(mu, x.z), __fmul_rn(mu, x.w));
+        *reinterpret_cast<float4*>(src + c) =
+            make_float4(__fmul_rn(mu, x.x), __fmul_rn(mu, x.y), __fmul_rn(mu, x.z), __fmul_rn(mu, x.w));
+      };
+      int c = lane * 4;
+      for (; c + 384 < a.m; c += 512) {
+        float4 x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) x[u] = *reinterpret_cast<const float4*>(src + c + 128 * u);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) put(c + 128 * u, x[u]);
       }
+      for (; c < a.m; c += 128) put(c, *reinterpret_cast<const float4*>(src + c));
     } else {
       for (int c = lane; c < a.m; c += 32) {
         const float x = src[c];
