@@ -12,8 +12,8 @@
 //   EPI_WUPD like EPI_GEN, but the epilogue adds alpha*acc into W[b][sel[b][r]][:] -- the
 //            Dion3 row update W[S,:] -= eta' O fused into the last product (Algorithm 4).
 //
-// CTA = 192 threads: warp 0 issues TMA loads, warp 1 owns TMEM and issues tcgen05.mma
-// (one thread), warps 2-5 drain the accumulators.  Tiles are BM=128 rows x BN (128 or 256)
+// CTA = 320 threads: warp 0 issues TMA loads, warp 1 owns TMEM and issues tcgen05.mma
+// (one thread), warps 2-9 drain the accumulators.  Tiles are BM=128 rows x BN (128 or 256)
 // columns, K in steps of 64 16-bit elements (one 128-byte swizzled row).  Two TMEM
 // accumulators let the epilogue of one tile overlap the main loop of the next.  Every
 // wait is bounded (clock64); a wait that gives up raises DION3_DEV_TIMEOUT and the CTA
@@ -32,11 +32,11 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-// Warp 0 issues TMA loads, warp 1 the MMAs, the remaining warps drain the accumulators: four
-// for the stored products, eight for the W row update, whose epilogue streams W through
-// registers and needs the extra warps to keep enough loads in flight.
+// Warp 0 issues TMA loads, warp 1 the MMAs, eight warps drain the accumulators: two per TMEM
+// lane quarter, which split each tile's 32-column chunks between them (a chunk's TMEM load,
+// conversion, staging and store is a dependent chain; two warps keep two chains in flight).
 template <int EPI>
-constexpr int epi_warps() { return EPI == EPI_WUPD ? 8 : 4; }
+constexpr int epi_warps() { return 8; }
 template <int EPI>
 constexpr int num_threads() { return 64 + 32 * epi_warps<EPI>(); }
 constexpr long long DEFAULT_SPIN = 4000000000LL;  // clock cycles (about 2 s)
@@ -341,8 +341,9 @@ __device__ __forceinline__ uint32_t stg_off(int row, int col) {
   return static_cast<uint32_t>(row * 64 + ((((col >> 3) ^ (row >> 1)) & 3) << 4) + ((col & 7) << 1));
 }
 
-// Epilogue of one tile for a 16-bit D (EPI_SYM or EPI_GEN).  Each warp owns 32 rows; every
-// 32-column chunk is converted, written into a swizzled staging block (and, for blocks below
+// Epilogue of one tile for a 16-bit D (EPI_SYM or EPI_GEN).  Each warp owns 32 rows and every
+// other 32-column chunk (its partner warp on the same TMEM lanes takes the rest); a chunk is
+// converted, written into a swizzled staging block (and, for blocks below
 // the diagonal, into a transposed block: lane pairs exchange halves so every shared store is a
 // full word), and stored with TMA bulk stores.  A diagonal block is made exactly symmetric in
 // shared memory (its upper half copied from the transposed lower half) and stored once.
@@ -350,7 +351,8 @@ __device__ __forceinline__ uint32_t stg_off(int row, int col) {
 // columns outside the matrix, and a warp whose rows all lie outside stores nothing.
 template <typename T, int BN, int EPI>
 __device__ __forceinline__ void epi_tile_tma(const KParams& p, const CUtensorMap* tmD, uint8_t* stg, int& buf,
-                                             uint32_t t_acc, int b, int mi, int nj, int ew, int lane, float ab) {
+                                             uint32_t t_acc, int b, int mi, int nj, int ew, int half, int lane,
+                                             float ab) {
   const int r0w = mi * BM + ew * 32;
   const int r = r0w + lane;
   const bool use_c = p.beta != 0.f;  // D = alpha acc + beta C (C has D's type and layout)
@@ -364,15 +366,15 @@ __device__ __forceinline__ void epi_tile_tma(const KParams& p, const CUtensorMap
     ++nch;
   }
   uint32_t cnx[16];
-  if (use_c && nch > 0) load_c32<T>(p, crow, nj * BN, cnx);
+  if (use_c && half < nch) load_c32<T>(p, crow, nj * BN + half * 32, cnx);
 #pragma unroll 1
-  for (int ch = 0; ch < nch; ++ch) {
+  for (int ch = half; ch < nch; ch += 2) {
     const int c0 = nj * BN + ch * 32;
     uint32_t cw[16];
     if (use_c) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) cw[i] = cnx[i];
-      if (ch + 1 < nch) load_c32<T>(p, crow, c0 + 32, cnx);  // prefetch the next chunk's C
+      if (ch + 2 < nch) load_c32<T>(p, crow, c0 + 64, cnx);  // prefetch this warp's next chunk of C
     }
     uint32_t v[32];
     __syncwarp();
@@ -742,7 +744,7 @@ __global__ void __launch_bounds__(num_threads<EPI>(), 1)
   } else {
     // ------------------------------------------------ epilogue (warps 2..5)
     const int ew = warp & 3;  // TMEM lanes 32*ew .. 32*ew+31
-    const int half = (warp - 2) >> 2;  // W row update: the two warps of a lane quarter split the chunks
+    const int half = (warp - 2) >> 2;  // the two warps of a lane quarter split the chunks
     uint8_t* stg = smem + Cf::STG_OFF + (warp - 2) * Cf::STG_WARP;
     int buf = 0;
     int acc = 0;
@@ -765,15 +767,15 @@ __global__ void __launch_bounds__(num_threads<EPI>(), 1)
       } else {
         if (p.d_type != FP32) {
           if (p.d_type == FP16)
-            epi_tile_tma<__half, BN, EPI>(p, &tmD, stg, buf, t_acc, b, mi, nj, ew, lane, ab);
+            epi_tile_tma<__half, BN, EPI>(p, &tmD, stg, buf, t_acc, b, mi, nj, ew, half, lane, ab);
           else
-            epi_tile_tma<__nv_bfloat16, BN, EPI>(p, &tmD, stg, buf, t_acc, b, mi, nj, ew, lane, ab);
+            epi_tile_tma<__nv_bfloat16, BN, EPI>(p, &tmD, stg, buf, t_acc, b, mi, nj, ew, half, lane, ab);
           done = true;
         }
       }
       if (!done) {
 #pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ++ch) {
+        for (int ch = half; ch < BN / 32; ch += 2) {
           const int c0 = nj * BN + ch * 32;
           if (c0 >= p.N) break;
           if (EPI == EPI_SYM && c0 > rmax_warp) break;
