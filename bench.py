@@ -268,7 +268,7 @@ def run_ours(args):
         "per_megabatch_ms": [{"shape": f"{x['B']}x{x['n']}x{x['m']}", "ms": sum(pm)} for x, pm in zip(mbs, per_mb)],
     }
     dominant = max(names, key=lambda n: ph[n])
-    launches_per_mb = d3.step_launch_count(T_ITERS, RESTARTS)
+    launches_per_mb = d3.step_launch_count(T_ITERS, RESTARTS, k_rows(MEGABATCHES[0][1]))
     if dominant == "gram_ns_products":
         n_launch = len(mbs) * (launches_per_mb - 3)
         achieved = flops / ph[dominant] / 1e9

@@ -333,11 +333,17 @@ def selftest_watchdog(spin_limit_cycles: int, status: torch.Tensor) -> None:
     _check(rc, "dion3_selftest_watchdog")
 
 
-def gram_core_launch_count(T: int, restart_after=()) -> int:
-    """Kernel launches of the Gram Newton-Schulz product chain (mirrors the library's driver):
-    R_0; per iteration Z, Q Z (not right after a (re)start), then either the restart's Q X and
-    X X^T or, before the last iteration, the two R-update products; finally Q X."""
-    rs = set(int(r) for r in restart_after)
+def gram_core_launch_count(T: int, restart_after=(), n: int | None = None, compute=torch.float16) -> int:
+    """Kernel launches of the Gram Newton-Schulz product chain (mirrors the library's driver).
+
+    n x n Gram matrices with n <= 128 and 16-bit iterates: R_0, one fused launch per restart
+    segment, the restart's Q X and X X^T, and the final Q X.  Otherwise: R_0; per iteration Z,
+    Q Z (not right after a (re)start), then either the restart's Q X and X X^T or, before the
+    last iteration, the two R-update products; finally Q X."""
+    rs = sorted(set(int(r) for r in restart_after))
+    if n is not None and n <= 128 and compute != torch.float32 and \
+            all(b - a <= 32 for a, b in zip([0] + rs, rs + [T])):
+        return 1 + (len(rs) + 1) + 2 * len(rs) + 1
     count, q_identity = 1, True
     for t in range(1, T + 1):
         count += 1
@@ -353,9 +359,10 @@ def gram_core_launch_count(T: int, restart_after=()) -> int:
     return count + 1
 
 
-def step_launch_count(T: int, restart_after=()) -> int:
-    """Kernel launches of one dion3_step call: momentum pass, selection, gather, product chain."""
-    return 3 + gram_core_launch_count(T, restart_after)
+def step_launch_count(T: int, restart_after=(), k: int | None = None, compute=torch.float16) -> int:
+    """Kernel launches of one dion3_step call (k selected rows): momentum pass, selection, gather,
+    product chain."""
+    return 3 + gram_core_launch_count(T, restart_after, k, compute)
 
 
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024  # DION3_NOALLOC_SCRATCH_BYTES in include/dion3.h

@@ -203,6 +203,43 @@ int run_core(const Core& c, cudaStream_t s) {
   const Mat none;
   int rc = sym(c.X0, c.X0, nn(Rb), c.m, 1.f, c.alpha2, none, 0.f, 0.f);
   if (rc) return rc;
+
+  // Small Gram matrices: every restart segment (its iterations from a (re)start up to the next
+  // restart or the end) is one fused launch that keeps R, Z and Q on chip.
+  bool fused = c.n <= 128 && c.cdt != FP32;
+  for (int i = 0, t0 = 1; fused && i <= c.n_restart; ++i) {
+    const int t1 = i < c.n_restart ? c.restarts[i] : c.T;
+    if (t1 - t0 + 1 > DION3_SEG_MAX_ITERS) fused = false;
+    t0 = t1 + 1;
+  }
+  if (fused) {
+    Mat Xcur = c.X0;
+    const float* xs = c.xscale;
+    int next_x = 0;
+    for (int i = 0, t0 = 1; i <= c.n_restart; ++i) {
+      const int t1 = i < c.n_restart ? c.restarts[i] : c.T;
+      rc = gram_segment(c.batch, c.n, nn(Rb), nn(Qb), t1 - t0 + 1, c.abc + 3 * (t0 - 1), c.status, s);
+      if (rc) return rc;
+      if (i < c.n_restart) {  // X <- Q X, R <- X X^T
+        Mat Xn;
+        Xn.ptr = c.ws + (next_x == 0 ? c.L.X1 : c.L.X2);
+        Xn.ld = c.L.ldm;
+        Xn.stride = static_cast<int64_t>(c.n) * c.L.ldm;
+        Xn.dtype = c.cdt;
+        next_x ^= 1;
+        rc = gen(nn(Qb), Xcur, 1.f, xs, EPI_GEN, Xn);
+        if (rc) return rc;
+        Xcur = Xn;
+        xs = nullptr;
+        rc = sym(Xcur, Xcur, nn(Rb), c.m, 1.f, nullptr, none, 0.f, 0.f);
+        if (rc) return rc;
+      }
+      t0 = t1 + 1;
+    }
+    if (c.wupd) return gen(nn(Qb), Xcur, c.w_alpha, xs, EPI_WUPD, none);
+    return gen(nn(Qb), Xcur, 1.f, xs, EPI_GEN, c.Out);
+  }
+
   bool q_identity = true;
   Mat Xcur = c.X0;
   const float* xs = c.xscale;

@@ -1005,6 +1005,10 @@ int launch(const GemmCall& g, cudaStream_t s) {
 
 }  // namespace
 
+bool tensor_map_16(CUtensorMap* map, const Mat& m, int rows, int cols, int batch, int box_cols, int box_rows) {
+  return make_map(map, m, rows, cols, batch, box_cols, box_rows);
+}
+
 int sm_count() {
   static int cache[64] = {0};
   int dev = 0;

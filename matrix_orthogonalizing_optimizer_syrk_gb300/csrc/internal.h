@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "dion3.h"
@@ -66,6 +67,17 @@ inline int gemm(const GemmCall& g, cudaStream_t s) {
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
+
+// 3-D TMA map over a 16-bit [batch][rows][cols] matrix (ld and stride from m), box
+// box_cols x box_rows, 128-byte swizzle (gemm_tc.cu).
+bool tensor_map_16(CUtensorMap* map, const Mat& m, int rows, int cols, int batch, int box_cols, int box_rows);
+
+// One restart segment of Gram Newton-Schulz on n x n Gram matrices, n <= 128, 16-bit (gram_small.cu):
+// from R (batch x n x n) run `iters` iterations with the (a, b, c) triples abc[0 .. 3 iters) and
+// write Q.  The R update after the segment's last iteration is skipped.
+#define DION3_SEG_MAX_ITERS 32
+int gram_segment(int batch, int n, const Mat& R, const Mat& Q, int iters, const float* abc, int* status,
+                 cudaStream_t s);
 
 // ---- elementwise / reduction launchers (elementwise.cu) ----
 // Per-row sum of squares of X (any dtype, any ld) into rowsq[b*n + i] (fp32).
