@@ -1023,8 +1023,8 @@ int sm_count() {
 int gemm_tc(const GemmCall& g, cudaStream_t s) {
   if (g.batch <= 0 || g.M <= 0 || g.N <= 0) return DION3_OK;
   if (g.beta != 0.f && (g.C.ptr == nullptr || g.C.dtype != g.D.dtype)) return DION3_EUNSUPPORTED;
-  // Pairs of 128-row blocks share each 256-column B tile through cluster multicast when there
-  // are at least two row blocks; otherwise one CTA per tile.
+  // Two CTAs (a cta_group::2 pair) compute each 256 x 256 tile when there are at least two row
+  // blocks, each staging half of the B tile; otherwise one CTA per 128-row tile.
   switch (g.epi) {
     case EPI_SYM: {
       // CTA pairs on 256 x 256 tiles, unless that leaves SMs idle: then 128 x 128 tiles, which

@@ -27,7 +27,7 @@ namespace {
 constexpr int SEG_THREADS = 128;
 constexpr int MAT_BYTES = 2 * 128 * 128;  // two 64-column panels of 128 rows x 128 bytes
 constexpr int PANEL_BYTES = 128 * 128;
-constexpr int NBUF = 4;                   // R, Z, Q, T (= R Z)
+constexpr int NBUF = 5;                   // R, Z, Q, T (= R Z), and the next matrix's R
 constexpr int SEG_SMEM = NBUF * MAT_BYTES + 1024 + 64;
 constexpr long long SEG_SPIN = 4000000000LL;
 
@@ -178,25 +178,27 @@ __global__ void __launch_bounds__(SEG_THREADS, 1)
     return true;
   };
 
+  // R of the next matrix is loaded into the spare buffer S while this one is computed; the
+  // buffers rotate (the old R becomes the next spare).
+  uint8_t* R = smem;
+  uint8_t* Z = smem + MAT_BYTES;
+  uint8_t* Q = smem + 2 * MAT_BYTES;
+  uint8_t* Tm = smem + 3 * MAT_BYTES;
+  uint8_t* S = smem + 4 * MAT_BYTES;
+  auto issue_load = [&](uint8_t* dst, int mat) {
+    ptx::mbar_arrive_expect_tx(bar_load, 2 * PANEL_BYTES);
+    ptx::tma_load_3d(ptx::smem_u32(dst), &tmR, bar_load, 0, 0, mat);
+    ptx::tma_load_3d(ptx::smem_u32(dst + PANEL_BYTES), &tmR, bar_load, 64, 0, mat);
+    load_pending = true;
+  };
+  if (tid == 0 && static_cast<int>(blockIdx.x) < p.batch) issue_load(R, blockIdx.x);
   for (int mat = blockIdx.x; ok && mat < p.batch; mat += gridDim.x) {
-    uint8_t* R = smem;
-    uint8_t* Z = smem + MAT_BYTES;
-    uint8_t* Q = smem + 2 * MAT_BYTES;
-    uint8_t* Tm = smem + 3 * MAT_BYTES;
-    if (tid == 0) {
-      // The previous matrix's Q store has to finish reading shared memory before the buffers
-      // are written again.
-      ptx::bulk_wait_all();
-      ptx::mbar_arrive_expect_tx(bar_load, 2 * PANEL_BYTES);
-      ptx::tma_load_3d(ptx::smem_u32(R), &tmR, bar_load, 0, 0, mat);
-      ptx::tma_load_3d(ptx::smem_u32(R + PANEL_BYTES), &tmR, bar_load, 64, 0, mat);
-      load_pending = true;
-    }
     if (!cta_wait(bar_load, ph_load)) {
       ok = false;
       break;
     }
     load_pending = false;
+    if (tid == 0 && mat + static_cast<int>(gridDim.x) < p.batch) issue_load(S, mat + gridDim.x);
     bool q_identity = true;
     for (int j = 0; j < p.iters; ++j) {
       const bool last = j + 1 == p.iters;
@@ -204,6 +206,8 @@ __global__ void __launch_bounds__(SEG_THREADS, 1)
       if (tid == 0) {
         mma_nn(tmem + 0, ptx::smem_u32(R), ptx::smem_u32(R), p.n16, p.idesc);
         ptx::tc_commit(bar_mma);
+        // The previous matrix's Q store must have read its buffer before anything is written.
+        if (j == 0) ptx::bulk_wait_read_0();
       }
       if (!cta_wait(bar_mma, ph_mma)) {
         ok = false;
@@ -253,6 +257,9 @@ __global__ void __launch_bounds__(SEG_THREADS, 1)
       if (p.n > 64) ptx::tma_store_3d(&tmQ, ptx::smem_u32(Q + PANEL_BYTES), 64, 0, mat);
       ptx::bulk_commit_group();
     }
+    uint8_t* t = R;
+    R = S;
+    S = t;
   }
   if (tid == 0) {
     // Let every issued copy and MMA finish before the shared memory and TMEM are released.
