@@ -609,14 +609,17 @@ int step_select(const StepArgs& s, cudaStream_t st) {
     return cudaGetLastError() == cudaSuccess ? DION3_OK : DION3_ECUDA;
   }
   const int smem = 11 * s.n + 16;
+  // One CTA per matrix; small matrices (many of them, e.g. MoE experts) get 256 threads so that
+  // several CTAs share an SM.
+  const int threads = s.n <= 2048 ? 256 : SEL_THREADS;
   if (s.norm_p == 1) {
     if (cudaFuncSetAttribute(select_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return DION3_ECUDA;
-    select_kernel<1><<<s.batch, SEL_THREADS, smem, st>>>(a);
+    select_kernel<1><<<s.batch, threads, smem, st>>>(a);
   } else {
     if (cudaFuncSetAttribute(select_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return DION3_ECUDA;
-    select_kernel<2><<<s.batch, SEL_THREADS, smem, st>>>(a);
+    select_kernel<2><<<s.batch, threads, smem, st>>>(a);
   }
   return cudaGetLastError() == cudaSuccess ? DION3_OK : DION3_ECUDA;
 }
