@@ -117,3 +117,37 @@ def test_megabatch_full_size_sampled(shape, count):
     for i in (0, count // 2, count - 1):
         ref = oracle.gram_ns(to64(X[i]), ABC, (2, 4))
         assert rel_frob(to64(O[i]), ref) <= 3e-2
+
+
+@pytest.mark.parametrize("n,m", [(128, 512), (65, 300), (64, 64), (127, 130)])
+@pytest.mark.parametrize("compute", [torch.float16, torch.bfloat16])
+def test_fused_segment_sizes(n, m, compute):
+    """Gram matrices up to 128 x 128 run each restart segment as one fused launch: both panel
+    boundaries (64, 65), the largest size (128) and a non-multiple of 16 (127)."""
+    X = synthetic.lowrank_plus_noise(n, m, seed=11 * n + m, dtype=torch.bfloat16, device=DEV)
+    O = d3.gram_ns(X, ABC, (2, 4), compute=compute)
+    torch.cuda.synchronize()
+    ref = oracle.gram_ns(to64(X), ABC, (2, 4))
+    assert rel_frob(to64(O), ref) <= 3e-2
+
+
+def test_segment_longer_than_fused_limit_falls_back():
+    """A 40-iteration segment (no restart) exceeds the fused kernel's 32-iteration table and runs
+    on the separate products; the cubic (1.5, -0.5, 0) converges to the polar factor."""
+    X = synthetic.lowrank_plus_noise(48, 200, seed=17, dtype=torch.bfloat16, device=DEV)
+    cubic = [(1.5, -0.5, 0.0)] * 40
+    O = d3.gram_ns(X, cubic, (), compute=torch.float16, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ref = oracle.gram_ns(to64(X), cubic, ())
+    assert rel_frob(to64(O), ref) <= 3e-2
+
+
+def test_many_small_matrices_batched():
+    """A batch larger than the grid: each CTA runs several matrices in turn (spare-buffer prefetch)."""
+    B, n, m = 400, 32, 96
+    X = synthetic.lowrank_batch(B, n, m, base_seed=900, dtype=torch.bfloat16, device=DEV)
+    O = d3.gram_ns(X, ABC, (2,))
+    torch.cuda.synchronize()
+    for i in (0, 151, 152, 303, 399):
+        ref = oracle.gram_ns(to64(X[i]), ABC, (2,))
+        assert rel_frob(to64(O[i]), ref) <= 3e-2
