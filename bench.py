@@ -197,6 +197,11 @@ def run_ours(args):
     peaks, peaks_kind = load_peaks()
 
     mbs = step_inputs(torch, synthetic, dev, rank)
+    # matrix 0 of each megabatch before any step: the oracle sample (timed on the host) and the
+    # inputs of the bench's own parity check
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu
+    sample0 = [(x["B"], x["W"][0].cpu().numpy().copy(), x["Gs"][0][0].float().cpu().numpy())
+               for x in mbs] if want_cpu else None
     ws_bytes = max(d3.workspace_bytes_step(x["B"], x["n"], x["m"], F[0], F[1], 1, torch.float16, len(RESTARTS))
                    for x in mbs)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
@@ -320,7 +325,7 @@ def run_ours(args):
         line["moe_step"] = bench_moe_step(torch, d3, synthetic, dev, peaks, peaks_kind)
         line["gram_ns_fp32"] = bench_gram_fp32(torch, d3, synthetic, dev)
     if rank == 0 and world == 1 and not args.no_cpu:
-        line["cpu_baseline"] = cpu_baseline(synthetic, torch)
+        line["cpu_baseline"], line["parity"] = cpu_baseline_and_parity(torch, d3, dev, sample0)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -587,13 +592,45 @@ def oracle_step_ms(samples) -> float:
     return total * 1e3
 
 
-def cpu_baseline(synthetic, torch):
-    samples = cpu_sample_inputs(synthetic, torch)
-    ms = oracle_step_ms(samples)
-    return {"value": ms, "unit": "ms per megabatch step (both 7B shape groups)", "cores": len(os.sched_getaffinity(0)),
-            "kind": "oracle",
+def cpu_baseline_and_parity(torch, d3, dev, sample0):
+    """The oracle's Dion3 step on matrix 0 of each megabatch (its first-step inputs, as generated
+    on the device), timed on the host cores and scaled by the megabatch sizes; and the same step
+    through the C ABI on those inputs (batch 1), compared with the oracle's result."""
+    import numpy as np
+
+    import oracle
+
+    total = 0.0
+    checks = []
+    for B, W0, G0 in sample0:
+        n, m = W0.shape
+        M0 = np.zeros((n, m), np.float32)
+        t0 = time.perf_counter()
+        W1, M1, S, _ = oracle.dion3_step(W0, M0, G0, F[0], F[1], mu=MU, eta=ETA, norm_p=1, abc=ABC,
+                                         restart_after=RESTARTS)
+        total += (time.perf_counter() - t0) * B
+        Wd = torch.from_numpy(W0).to(dev).unsqueeze(0).contiguous()
+        Md = torch.zeros((1, n, m), dtype=torch.float32, device=dev)
+        Gd = torch.from_numpy(G0).to(device=dev, dtype=torch.bfloat16).unsqueeze(0).contiguous()
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        sel = d3.step(Wd, Md, Gd, f=F, mu=MU, eta=ETA, norm_p=1, abc=ABC, restart_after=RESTARTS,
+                      compute=torch.float16, status=status)
+        torch.cuda.synchronize()
+        dW = Wd[0].double().cpu().numpy() - W0
+        ref = W1 - W0
+        checks.append({"shape": f"{n}x{m}", "rows_selected_equal": bool(np.array_equal(sel[0].cpu().numpy(), S)),
+                       "M_bit_exact": bool(np.array_equal(Md[0].cpu().numpy().view(np.uint32), M1.view(np.uint32))),
+                       "dW_rel_frob": float(np.linalg.norm(dW - ref) / np.linalg.norm(ref)),
+                       "device_status": int(status.item())})
+        del Wd, Md, Gd
+    base = {"value": total * 1e3, "unit": "ms per megabatch step (both 7B shape groups)",
+            "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
             "sample": "one oracle Dion3 step (float64, exact keys) on matrix 0 of each megabatch "
-                      "(4096x4096 and 4096x11008 at M=0), scaled by the megabatch sizes 128 and 96"}
+                      "(4096x4096 and 4096x11008, first-step inputs, M=0), scaled by the megabatch sizes 128 and 96"}
+    parity = {"against": "the oracle's step on matrix 0 of each megabatch (the cpu_baseline sample), same inputs, "
+                         "run through the C ABI with batch 1",
+              "tolerance": {"rows": "bit-exact", "M": "bit-exact", "dW_rel_frob": 3e-2}, "checks": checks}
+    return base, parity
 
 
 def run_reference(args):

@@ -341,6 +341,18 @@ __device__ __forceinline__ uint32_t stg_off(int row, int col) {
   return static_cast<uint32_t>(row * 64 + ((((col >> 3) ^ (row >> 1)) & 3) << 4) + ((col & 7) << 1));
 }
 
+// Row `lane` of a staged 32 x 32 block (layout of stg_off) into D[b][row0 + lane][col0 ..], clipped
+// to the matrix; used where a TMA store would write past the end of a row.  Kept out of line:
+// it runs only for blocks on a ragged right edge.
+__device__ __noinline__ void store_block_plain(const KParams& p, int b, const uint8_t* blk, int row0, int col0,
+                                               int lane) {
+  const int row = row0 + lane;
+  if (row >= p.M) return;
+  uint16_t* drow = static_cast<uint16_t*>(p.D) + static_cast<long long>(b) * p.sD + static_cast<long long>(row) * p.ldd;
+  for (int c = col0; c < p.N && c < col0 + 32; ++c)
+    drow[c] = *reinterpret_cast<const uint16_t*>(blk + stg_off(lane, c - col0));
+}
+
 // Epilogue of one tile for a 16-bit D (EPI_SYM or EPI_GEN).  Each warp owns 32 rows and every
 // other 32-column chunk (its partner warp on the same TMEM lanes takes the rest); a chunk is
 // converted, written into a swizzled staging block (and, for blocks below
@@ -435,11 +447,18 @@ __device__ __forceinline__ void epi_tile_tma(const KParams& p, const CUtensorMap
     }
     ptx::fence_proxy_async_smem();
     __syncwarp();
+    // A TMA store writes whole 16-byte units of a row, so a block whose columns run past a row
+    // end that is not 16-byte aligned is written with plain stores instead (lane = block row).
+    const bool ragged = (p.N & 7) != 0;
+    const bool blk_plain = ragged && c0 + 32 > p.N;
+    const bool tr_plain = ragged && below && r0w + 32 > p.N;
     if (lane == 0) {
-      ptx::tma_store_3d(tmD, ptx::smem_u32(S), c0, r0w, b);
-      if (below) ptx::tma_store_3d(tmD, ptx::smem_u32(Tt), r0w, c0, b);
+      if (!blk_plain) ptx::tma_store_3d(tmD, ptx::smem_u32(S), c0, r0w, b);
+      if (below && !tr_plain) ptx::tma_store_3d(tmD, ptx::smem_u32(Tt), r0w, c0, b);
       ptx::bulk_commit_group();
     }
+    if (blk_plain) store_block_plain(p, b, S, r0w, c0, lane);
+    if (tr_plain) store_block_plain(p, b, Tt, c0, r0w, lane);
     buf ^= 1;
   }
 }
