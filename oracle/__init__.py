@@ -36,7 +36,7 @@ from .newton_schulz import (
     odd_poly,
     theorem2_scalar,
 )
-from .dion3 import ceil_k, dion3_step, exact_row_keys, top_k_rows
+from .dion3 import ceil_k, dion3_step, dion3_step_cols, exact_row_keys, top_k_rows
 from .sym_gemm import sym_gemm
 
 __all__ = [
@@ -44,6 +44,7 @@ __all__ = [
     "ceil_k",
     "composite_scalar",
     "dion3_step",
+    "dion3_step_cols",
     "exact_row_keys",
     "flop_count",
     "gram_ns",

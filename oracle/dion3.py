@@ -13,6 +13,9 @@ Sources (page title, section):
   The step takes the Muon-equivalent eta and applies eta' itself; the weight
   decay factor uses eta' as well.
 * Same page, "existing work": k = ceil(f n), rows taken as they are.
+* "Dion3" summary (m.montaan.com), update-rule paragraph: f is the fraction of rows (or columns)
+  selected.  ``dion3_step_cols`` takes a matrix stored m x n with the short side n as its
+  columns and selects columns: by definition the row step applied to the transpose.
 * Same page, "limitations" and "future directions": choosing S at random
   works about as well as the l1 rule, and a set S that does not depend on M
   is what lets a data-parallel run synchronise only M[S, :].  ``rows``
@@ -117,3 +120,20 @@ def dion3_step(W, M, G, f_num: int, f_den: int, mu: float, eta: float, wd: float
     mu32 = np.float64(np.float32(mu))
     M2[S] = (mu32 * M1[S].astype(np.float64)).astype(np.float32)
     return W1, M2, S, O
+
+
+def dion3_step_cols(W, M, G, f_num: int, f_den: int, mu: float, eta: float, wd: float = 0.0,
+                    norm_p: int = 1, abc=None, restart_after=(), eps: float = 1e-7, cols=None):
+    """One Dion3 step on a matrix stored m x n (n <= m) that selects columns.
+
+    ``cols``: optional caller-chosen column set.  Returns (W_new float64 m x n, M_new fp32 m x n,
+    S int64 ascending column indices, O float64 k x m).  The row step of the transposed matrix,
+    transposed back.
+    """
+    W = np.asarray(W)
+    M = np.asarray(M, dtype=np.float32)
+    G = np.asarray(G)
+    W1t, M1t, S, O = dion3_step(W.T, M.T, G.T, f_num, f_den, mu=mu, eta=eta, wd=wd, norm_p=norm_p, abc=abc,
+                                restart_after=restart_after, eps=eps, rows=cols)
+    return W1t.T, np.ascontiguousarray(M1t.T), S, O
+

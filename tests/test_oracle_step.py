@@ -205,3 +205,42 @@ def test_given_rows_validated(rows, jordan):
     W, M, G = _step_inputs(24, 40, seed=13)
     with pytest.raises(ValueError):
         oracle.dion3_step(W, M, G, 1, 4, mu=0.95, eta=0.01, abc=[jordan] * 5, rows=rows)
+
+
+def test_column_step_error_feedback_and_polar(jordan):
+    """Column selection on a matrix stored m x n: the k columns of largest exact l1 norm (checked
+    with exact fractions), M[:, S] = fl32(mu (M+G)), other columns M+G bit for bit, W changes only
+    on S, by eta' times the SVD polar factor of M[:, S] (cubic iteration run to convergence)."""
+    m, n = 30, 12
+    rng = np.random.default_rng(21)
+    W = (rng.standard_normal((m, n)) * 0.02).astype(np.float32)
+    M = (rng.standard_normal((m, n)) * 0.05).astype(np.float32)
+    G = rng.standard_normal((m, n)).astype(np.float32)
+    G = (G.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32)
+    mu, eta, f = 0.9, 0.01, (1, 3)
+    cubic = [(1.5, -0.5, 0.0)] * 60
+    W1, M1, S, _ = oracle.dion3_step_cols(W, M, G, *f, mu=mu, eta=eta, abc=cubic)
+    summed = M + G
+    keys = [sum(Fraction(float(abs(x))) for x in summed[:, j]) for j in range(n)]
+    k = oracle.ceil_k(n, *f)
+    order = sorted(range(n), key=lambda j: (-keys[j], j))
+    assert list(S) == sorted(order[:k])
+    sel = np.zeros(n, bool)
+    sel[S] = True
+    assert np.array_equal(M1[:, ~sel].view(np.uint32), summed[:, ~sel].view(np.uint32))
+    assert np.array_equal(M1[:, sel].view(np.uint32), (np.float32(mu) * summed)[:, sel].view(np.uint32))
+    assert np.array_equal(W1[:, ~sel], W[:, ~sel].astype(np.float64))
+    U, _, Vt = np.linalg.svd(summed[:, S].T.astype(np.float64), full_matrices=False)
+    eta_p = eta * math.sqrt(f[1] / f[0])
+    np.testing.assert_allclose((W1 - W.astype(np.float64))[:, S], (-eta_p * (U @ Vt)).T, rtol=0, atol=1e-10)
+
+
+def test_column_step_given_columns(jordan):
+    m, n = 20, 8
+    rng = np.random.default_rng(22)
+    W = (rng.standard_normal((m, n)) * 0.02).astype(np.float32)
+    M = np.zeros((m, n), np.float32)
+    G = rng.standard_normal((m, n)).astype(np.float32)
+    W1, M1, S, _ = oracle.dion3_step_cols(W, M, G, 1, 4, mu=0.95, eta=0.01, abc=[jordan] * 5, cols=[6, 1])
+    assert list(S) == [1, 6]
+    assert np.array_equal(W1[:, [0, 2, 3, 4, 5, 7]], W[:, [0, 2, 3, 4, 5, 7]].astype(np.float64))
