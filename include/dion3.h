@@ -244,6 +244,36 @@ int dion3_step_timed(int batch, int n, int m,
                      int* status_dev, void* stream, void* const* events, int n_events);
 
 /*
+ * dion3_step_cols_workspace_bytes -- bytes of workspace dion3_step_cols needs.  0 for invalid sizes.
+ */
+size_t dion3_step_cols_workspace_bytes(int batch, int m, int n, int f_num, int f_den, int norm_p,
+                                       int compute_dtype, int n_restart);
+
+/*
+ * dion3_step_cols -- one Dion3 step on matrices stored un-oriented, [batch][m][n] with the short
+ * side n as columns (n <= m), selecting columns: [D3m] update-rule paragraph (f is the fraction
+ * of rows or columns selected) with everything else as dion3_step.  In exact arithmetic it is
+ * dion3_step on the transposed matrices, transposed back:
+ *   M <- M + G;  key_j = sum_i |M_ij| (norm_p = 1) or sum_i M_ij^2 (norm_p = 2);
+ *   S = the k = ceil(f n) columns with the largest exact keys (ties to the lower index);
+ *   O = GramNS(M[:, S]^T) (k x m);  W <- (1 - eta' wd) W;  W[:, S] <- W[:, S] - eta' O^T;
+ *   M[:, S] <- mu M[:, S].
+ *   W, M : fp32 [batch][m][n] contiguous (ld = n, stride = m*n), updated in place.
+ *   G    : [batch][m][n] contiguous, g_dtype as dion3_step.
+ *   sel_out : int32 [batch][k], ascending column indices (read when norm_p = DION3_SELECT_GIVEN).
+ *   The columns are gathered and scattered through shared-memory transposes; O passes through
+ *   the workspace in the compute dtype (one rounding that dion3_step's fused update avoids).
+ *   Limits: n <= 16384, m <= 65536, batch <= 65535.  Errors and device flags as dion3_step.
+ */
+int dion3_step_cols(int batch, int m, int n,
+                    float* W, float* M, const void* G, int g_dtype,
+                    int f_num, int f_den, float mu, float eta, float wd, int norm_p,
+                    int T, const float* abc, const int* restart_after, int n_restart, float eps,
+                    int compute_dtype, int32_t* sel_out,
+                    void* workspace, size_t workspace_bytes,
+                    int* status_dev, void* stream);
+
+/*
  * dion3_step_dev -- dion3_step with the hyperparameters read on the device, for CUDA-graph
  * capture: a graph captured around one call replays every later step with whatever values
  * hyper_dev holds when it runs (a learning-rate schedule without re-capture).  [D3] "method

@@ -53,6 +53,10 @@ SIGNATURES = {
     "dion3_step_timed": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_f, _c_f,
                                   _c_f, _c_int, _c_int, ctypes.POINTER(_c_f), ctypes.POINTER(_c_int), _c_int, _c_f,
                                   _c_int, _c_p, _c_p, _c_sz, _c_p, _c_p, ctypes.POINTER(_c_p), _c_int]),
+    "dion3_step_cols_workspace_bytes": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "dion3_step_cols": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_f, _c_f, _c_f,
+                                 _c_int, _c_int, ctypes.POINTER(_c_f), ctypes.POINTER(_c_int), _c_int, _c_f, _c_int,
+                                 _c_p, _c_p, _c_sz, _c_p, _c_p]),
     "dion3_step_dev": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_p, _c_int,
                                 _c_int, _c_int, ctypes.POINTER(_c_f), ctypes.POINTER(_c_int), _c_int, _c_f, _c_int,
                                 _c_p, _c_p, _c_sz, _c_p, _c_p]),
@@ -324,6 +328,54 @@ def step(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, f=(1, 4), mu: float 
                                     _dtype_code(compute), _ptr(sel_out), _ptr(workspace), workspace.numel(),
                                     _ptr(status), _stream_ptr(M.device), handles, len(events))
         _check(rc, "dion3_step_timed")
+    return sel_out
+
+
+def workspace_bytes_step_cols(batch: int, m: int, n: int, f_num: int, f_den: int, norm_p: int, compute,
+                              n_restart: int) -> int:
+    return int(lib().dion3_step_cols_workspace_bytes(batch, m, n, f_num, f_den, norm_p, _dtype_code(compute),
+                                                     n_restart))
+
+
+def step_cols(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, f=(1, 4), mu: float = 0.95, eta: float = 0.01,
+              wd: float = 0.0, norm_p: int = 1, abc=None, restart_after=(2,), eps: float = 1e-7,
+              compute=torch.float16, sel_out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+              status: torch.Tensor | None = None, cols: torch.Tensor | None = None) -> torch.Tensor:
+    """One Dion3 step on [batch, m, n] (or [m, n]) contiguous W, M (fp32) and G stored with the
+    short side n as columns (n <= m); selects k = ceil(f n) columns and returns them.  ``cols``:
+    optional caller-chosen columns, int32 [batch, k] ascending."""
+    for t, name in ((W, "W"), (M, "M"), (G, "G")):
+        _cuda(t, name)
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if W.dtype != torch.float32 or M.dtype != torch.float32:
+        raise TypeError("W and M are fp32 state")
+    if W.shape != M.shape or G.shape != M.shape:
+        raise ValueError("W, M, G must have the same shape")
+    batch = 1 if M.dim() == 2 else M.shape[0]
+    m, n = M.shape[-2], M.shape[-1]
+    f_num, f_den = f
+    k = k_of(n, f_num, f_den)
+    if k < 0:
+        raise ValueError("need 0 < f <= 1")
+    shape = (k,) if M.dim() == 2 else (batch, k)
+    if sel_out is None:
+        sel_out = torch.empty(shape, dtype=torch.int32, device=M.device)
+    if cols is not None:
+        _cuda(cols, "cols")
+        if cols.dtype != torch.int32 or tuple(cols.shape) != shape:
+            raise ValueError(f"cols must be int32 of shape {shape}")
+        if cols.data_ptr() != sel_out.data_ptr():
+            sel_out.copy_(cols)
+        norm_p = SELECT_GIVEN
+    T, flat, rarr, nr = _abc_arrays(abc, restart_after)
+    need = workspace_bytes_step_cols(batch, m, n, f_num, f_den, norm_p, compute, nr)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=M.device)
+    rc = lib().dion3_step_cols(batch, m, n, _ptr(W), _ptr(M), _ptr(G), _dt(G), f_num, f_den, float(mu), float(eta),
+                               float(wd), norm_p, T, flat, rarr, nr, float(eps), _dtype_code(compute), _ptr(sel_out),
+                               _ptr(workspace), workspace.numel(), _ptr(status), _stream_ptr(M.device))
+    _check(rc, "dion3_step_cols")
     return sel_out
 
 

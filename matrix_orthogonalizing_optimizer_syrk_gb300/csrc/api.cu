@@ -89,11 +89,14 @@ NsLayout ns_layout(int batch, int n, int m, int cdt) {
 
 struct StepLayout {
   size_t key_lo, key_hi, exact, rowsq, scale, xs;
+  size_t part_s, part_q, obuf;  // column selection: chunk sums of the column keys, and O
+  int nchunk;
   CoreLayout core;
   size_t total;
 };
 
-StepLayout step_layout(int batch, int n, int m, int k, int norm_p, int cdt, int n_restart) {
+// n keys (rows, or columns with `cols`), each a vector of m entries.
+StepLayout step_layout(int batch, int n, int m, int k, int norm_p, int cdt, int n_restart, bool cols = false) {
   StepLayout L{};
   Carve cv;
   L.key_lo = cv.take(sizeof(float) * static_cast<size_t>(batch) * n);
@@ -102,6 +105,12 @@ StepLayout step_layout(int batch, int n, int m, int k, int norm_p, int cdt, int 
   L.rowsq = cv.take(sizeof(float) * static_cast<size_t>(batch) * n);
   L.scale = cv.take(sizeof(float) * batch);
   L.xs = cv.take(static_cast<size_t>(batch) * k * round_up(m, 8) * dtype_size(cdt));
+  if (cols) {
+    L.nchunk = (m + STEP_COL_CHUNK - 1) / STEP_COL_CHUNK;
+    L.part_s = cv.take(sizeof(float) * static_cast<size_t>(batch) * L.nchunk * n);
+    L.part_q = cv.take(sizeof(float) * static_cast<size_t>(batch) * L.nchunk * n);
+    L.obuf = cv.take(static_cast<size_t>(batch) * k * round_up(m, 8) * dtype_size(cdt));
+  }
   core_layout(cv, L.core, batch, k, m, cdt, n_restart);
   L.total = round_up(static_cast<int64_t>(cv.off), WS_ALIGN);
   return L;
@@ -557,7 +566,7 @@ int step_impl(int batch, int n, int m, float* W, float* M, const void* G, int g_
               float mu, float eta, float wd, const float* hyper_dev, bool decay, int norm_p, int T, const float* abc,
               const int* restart_after, int n_restart, float eps, int compute_dtype, int32_t* sel_out,
               void* workspace, size_t workspace_bytes, int* status_dev, void* stream, void* const* events,
-              int n_events) {
+              int n_events, bool cols = false) {
   if (n_events < 0 || (n_events > 0 && events == nullptr)) return DION3_EINVAL;
   if (batch < 0 || n < 0 || m < 0) return DION3_EINVAL;
   if (!dtype_valid(g_dtype) || !dtype_valid(compute_dtype)) return DION3_EINVAL;
@@ -573,7 +582,8 @@ int step_impl(int batch, int n, int m, float* W, float* M, const void* G, int g_
   if (W == nullptr || M == nullptr || G == nullptr || sel_out == nullptr) return DION3_EINVAL;
   if (!al16(W) || !al16(M) || !al16(G) || !al16(sel_out)) return DION3_EALIGN;
   if (hyper_dev != nullptr && (reinterpret_cast<uintptr_t>(hyper_dev) & 3u) != 0) return DION3_EALIGN;
-  const StepLayout L = step_layout(batch, n, m, k, norm_p, compute_dtype, n_restart);
+  if (cols && batch > 65535) return DION3_EUNSUPPORTED;
+  const StepLayout L = step_layout(batch, n, m, k, norm_p, compute_dtype, n_restart, cols);
   if (workspace == nullptr || workspace_bytes < L.total) return DION3_EWORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & (WS_ALIGN - 1)) != 0) return DION3_EALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -611,13 +621,19 @@ int step_impl(int batch, int n, int m, float* W, float* M, const void* G, int g_
   sa.scale = reinterpret_cast<float*>(ws + L.scale);
   sa.eps = eps;
   sa.status = status_dev;
+  sa.cols = cols;
+  if (cols) {
+    sa.part_s = reinterpret_cast<float*>(ws + L.part_s);
+    sa.part_q = reinterpret_cast<float*>(ws + L.part_q);
+    sa.nchunk = L.nchunk;
+  }
 
   // Phase boundaries for the caller's timing events (0: start ... 4: end).
   auto mark = [&](int i) {
     if (i < n_events && events[i] != nullptr) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
   };
   mark(0);
-  int rc = step_momentum_keys(sa, s);
+  int rc = cols ? step_colkeys(sa, s) : step_momentum_keys(sa, s);
   if (rc) return rc;
   mark(1);
   rc = step_select(sa, s);
@@ -628,7 +644,7 @@ int step_impl(int batch, int n, int m, float* W, float* M, const void* G, int g_
     mark(4);
     return DION3_OK;
   }
-  rc = step_gather(sa, s);
+  rc = cols ? step_gather_cols(sa, s) : step_gather(sa, s);
   if (rc) return rc;
   mark(3);
   Core c;
@@ -643,7 +659,8 @@ int step_impl(int batch, int n, int m, float* W, float* M, const void* G, int g_
   c.abc = abc;
   c.restarts = restart_after;
   c.n_restart = n_restart;
-  c.wupd = true;
+  c.wupd = !cols;  // columns: O goes to the workspace and a transposing pass updates W
+  if (cols) c.Out = Mat{ws + L.obuf, ldm, static_cast<int64_t>(k) * ldm, compute_dtype};
   c.W = W;
   c.ldw = m;
   c.sW = static_cast<int64_t>(n) * m;
@@ -657,6 +674,10 @@ int step_impl(int batch, int n, int m, float* W, float* M, const void* G, int g_
   c.status = status_dev;
   rc = run_core(c, s);
   if (rc) return rc;
+  if (cols) {
+    rc = step_scatter_cols(sa, ws + L.obuf, ldm, c.w_alpha, c.eta_dev, c.eta_scale, s);
+    if (rc) return rc;
+  }
   mark(4);
   return DION3_OK;
 }
@@ -672,6 +693,25 @@ int dion3_step_timed(int batch, int n, int m, float* W, float* M, const void* G,
   return step_impl(batch, n, m, W, M, G, g_dtype, f_num, f_den, mu, eta, wd, nullptr, false, norm_p, T, abc,
                    restart_after, n_restart, eps, compute_dtype, sel_out, workspace, workspace_bytes, status_dev,
                    stream, events, n_events);
+}
+
+size_t dion3_step_cols_workspace_bytes(int batch, int m, int n, int f_num, int f_den, int norm_p, int compute_dtype,
+                                       int n_restart) {
+  if (batch < 0 || n < 0 || m < n || n_restart < 0) return 0;
+  if (norm_p != DION3_SELECT_GIVEN && norm_p != 1 && norm_p != 2) return 0;
+  if (!dtype_valid(compute_dtype)) return 0;
+  const int k = dion3_k(n, f_num, f_den);
+  if (k < 0) return 0;
+  return step_layout(batch, n, m, k, norm_p, compute_dtype, n_restart, true).total;
+}
+
+int dion3_step_cols(int batch, int m, int n, float* W, float* M, const void* G, int g_dtype, int f_num, int f_den,
+                    float mu, float eta, float wd, int norm_p, int T, const float* abc, const int* restart_after,
+                    int n_restart, float eps, int compute_dtype, int32_t* sel_out, void* workspace,
+                    size_t workspace_bytes, int* status_dev, void* stream) {
+  return step_impl(batch, n, m, W, M, G, g_dtype, f_num, f_den, mu, eta, wd, nullptr, false, norm_p, T, abc,
+                   restart_after, n_restart, eps, compute_dtype, sel_out, workspace, workspace_bytes, status_dev,
+                   stream, nullptr, 0, true);
 }
 
 int dion3_step_dev(int batch, int n, int m, float* W, float* M, const void* G, int g_dtype, int f_num, int f_den,

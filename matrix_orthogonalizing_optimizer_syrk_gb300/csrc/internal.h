@@ -115,10 +115,25 @@ struct StepArgs {
   float* scale;  // [batch]: 1 / (||M[S,:]||_F + eps)
   float eps;
   int* status;
+  // Column selection: W, M, G stored [batch][m][n] and the n keys belong to columns (each a
+  // vector of m entries).  Pass A then writes per-chunk column partial sums (part_s, part_q:
+  // [batch][nchunk][n]) that a finalize kernel turns into keys and column sums of squares.
+  bool cols = false;
+  float* part_s = nullptr;
+  float* part_q = nullptr;
+  int nchunk = 0;
 };
 int step_momentum_keys(const StepArgs& a, cudaStream_t s);
 int step_select(const StepArgs& a, cudaStream_t s);
 int step_gather(const StepArgs& a, cudaStream_t s);
+// Column selection only (step_cols.cu): pass A with column keys (and its finalize), and pass C.
+int step_colkeys(const StepArgs& a, cudaStream_t s);
+int step_gather_cols(const StepArgs& a, cudaStream_t s);
+// Column selection only: W[b][i][S_j] += alpha * O[b][j][i] for the k x m matrices O (compute
+// dtype, leading dimension ldo); alpha is float(-double(*eta_dev) * eta_scale) when eta_dev is set.
+int step_scatter_cols(const StepArgs& a, const void* O, int64_t ldo, float alpha, const float* eta_dev,
+                      double eta_scale, cudaStream_t s);
+constexpr int STEP_COL_CHUNK = 256;  // rows per partial sum of a column key
 int step_exact_limbs(int norm_p);
 
 // Watchdog self-test kernel (gemm_tc.cu).

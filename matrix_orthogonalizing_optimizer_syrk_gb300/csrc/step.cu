@@ -260,6 +260,7 @@ __device__ __forceinline__ int limbs_cmp(const uint64_t* a, const uint64_t* b) {
 struct BArgs {
   int n, m, k;
   const float* M;
+  long long kstride, estride;  // key i's vector: M + b*n*m + i*kstride, entries estride apart
   const float* key_lo;
   const float* key_hi;
   uint64_t* exact;
@@ -353,10 +354,11 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const BArgs a) {
       const int row = amb[j];
       for (int q = tid; q < NB; q += bd) bkt[q] = 0ull;
       __syncthreads();
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(a.M + (static_cast<long long>(b) * n + row) * a.m);
+      const uint32_t* src =
+          reinterpret_cast<const uint32_t*>(a.M + static_cast<long long>(b) * n * a.m + row * a.kstride);
       for (int base = 0; base < a.m; base += bd) {
         const int e = base + tid;
-        const uint32_t bits = e < a.m ? src[e] : 0u;
+        const uint32_t bits = e < a.m ? src[e * a.estride] : 0u;
         const uint32_t e8 = (bits >> 23) & 255u;
         uint32_t mant = (bits & 0x7FFFFFu) | (e8 ? 0x800000u : 0u);
         if (e8 == 255u) {
@@ -603,6 +605,8 @@ int step_select(const StepArgs& s, cudaStream_t st) {
   a.scale = s.scale;
   a.eps = s.eps;
   a.status = s.status;
+  a.kstride = s.cols ? 1 : s.m;
+  a.estride = s.cols ? s.n : 1;
   if (s.norm_p == DION3_SELECT_GIVEN) {
     if (s.k <= 0) return DION3_OK;
     given_kernel<<<s.batch, 256, 0, st>>>(a);

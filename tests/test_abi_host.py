@@ -208,3 +208,18 @@ def test_given_selection_mode_accepted(L):
     assert _step(L, p=3) == 1
     assert d3.workspace_bytes_step(2, 64, 128, 1, 4, 0, 0, 2) > 0
     assert d3.workspace_bytes_step(2, 64, 128, 1, 4, 0, 0, 2) < d3.workspace_bytes_step(2, 64, 128, 1, 4, 1, 0, 2)
+
+
+def test_step_cols_validation(L):
+    r = (ctypes.c_int * 1)(2)
+
+    def call(batch=1, m=128, n=64, W=FAKE, ws=FAKE, wsb=1 << 40, p=1):
+        return L.dion3_step_cols(batch, m, n, W, FAKE, FAKE, 0, 1, 4, 0.95, 0.01, 0.0, p, 5, _abc(5), r, 1, 1e-7, 0,
+                                 FAKE, ws, wsb, NULL, NULL)
+
+    assert call(m=32, n=64) == 1          # n > m
+    assert call(W=NULL) == 1
+    assert call(ws=NULL) == 3
+    assert call(p=3) == 1
+    assert call(batch=70000, wsb=16) == 2
+    assert d3.workspace_bytes_step_cols(2, 128, 64, 1, 4, 1, 0, 2) > d3.workspace_bytes_step(2, 64, 128, 1, 4, 1, 0, 2)
