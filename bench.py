@@ -323,6 +323,7 @@ def run_ours(args):
         line["gram_ns"] = bench_gram_ns(torch, d3, synthetic, dev, peaks, peaks_kind)
         line["sym_gemm"] = bench_sym_gemm(torch, d3, synthetic, dev, peaks, peaks_kind)
         line["moe_step"] = bench_moe_step(torch, d3, synthetic, dev, peaks, peaks_kind)
+        line["moe_w2_columns"] = bench_moe_w2_cols(torch, d3, synthetic, dev)
         line["gram_ns_fp32"] = bench_gram_fp32(torch, d3, synthetic, dev)
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"], line["parity"] = cpu_baseline_and_parity(torch, d3, dev, sample0)
@@ -507,6 +508,29 @@ def bench_moe_step(torch, d3, synthetic, dev, peaks, peaks_kind):
            "peak_source": f"{peaks_kind} hbm_gbs"}
     del W, M, Gs, ws
     torch.cuda.empty_cache()
+    return out
+
+
+def bench_moe_w2_cols(torch, d3, synthetic, dev):
+    """The 1024 MoE w2 matrices in their stored layout (2048 x 768, short side = columns), f = 1/8:
+    dion3_step_cols, beside dion3_step on the same matrices oriented (768 x 2048)."""
+    B, m, n = 1024, 2048, 768
+    fk = (1, 8)
+    out = {"workload": "MoE w2: 1024 x (2048 x 768) stored, f=1/8 (k=96 columns), T=5 Jordan, restarts 2,4, "
+                       "fp16 iterates"}
+    for name, shape, fn_name in (("columns_stored_2048x768", (B, m, n), "step_cols"),
+                                 ("rows_oriented_768x2048", (B, n, m), "step")):
+        W = synthetic.gaussian(shape, seed=6100, std=0.02, device=dev)
+        M = torch.zeros(shape, dtype=torch.float32, device=dev)
+        G = synthetic.lowrank_batch(B, shape[1], shape[2], base_seed=6200, dtype=torch.bfloat16, device=dev)
+        fn = getattr(d3, fn_name)
+        call = lambda: fn(W, M, G, f=fk, mu=MU, eta=ETA, abc=ABC, restart_after=RESTARTS)  # noqa: E731
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        out[name + "_ms"] = _time_calls(torch, call, 5)
+        del W, M, G
+        torch.cuda.empty_cache()
     return out
 
 

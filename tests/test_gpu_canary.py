@@ -128,3 +128,18 @@ def test_sym_gemm_writes_stay_inside(n, k, beta):
     d3.sym_gemm(A, C=C if beta else None, beta=beta, out=D[0])
     torch.cuda.synchronize()
     assert go.intact() and pad_intact(full, n)
+
+
+def test_step_cols_writes_stay_inside():
+    B, m, n, f = 2, 600, 72, (1, 4)
+    k = d3.k_of(n, *f)
+    gW, W = guarded_tensor((B, m, n), torch.float32, synthetic.gaussian((B, m, n), seed=41, std=0.02, device=DEV))
+    gM, M = guarded_tensor((B, m, n), torch.float32, synthetic.gaussian((B, m, n), seed=42, std=0.01, device=DEV))
+    G = synthetic.lowrank_batch(B, m, n, base_seed=1600, dtype=torch.bfloat16, device=DEV)
+    gS, sel = guarded_tensor((B, k), torch.int32)
+    gws = Guarded(d3.workspace_bytes_step_cols(B, m, n, f[0], f[1], 1, torch.float16, 2))
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    d3.step_cols(W, M, G, f=f, abc=ABC, restart_after=(2, 4), sel_out=sel, workspace=gws.inner(), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert gW.intact() and gM.intact() and gS.intact() and gws.intact()
