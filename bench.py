@@ -58,7 +58,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sub", action="store_true", help="skip the Gram-NS and sym-GEMM sub-measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
-    ap.add_argument("--case", choices=["gram_small", "step_small", "sym_gemm", "moe", "moe_gram", "fp32"], default=None,
+    ap.add_argument("--case", choices=["gram_small", "step_small", "sym_gemm", "moe", "moe_gram", "moe_w2_cols", "fp32"],
+                    default=None,
                     help="run one small profiling case (a few GB, inputs larger than L2) instead of the bench")
     return ap.parse_args()
 
@@ -722,6 +723,12 @@ def run_case(args):
         B, n, m = 768, 96, 2048  # a quarter of the MoE megabatch's selected rows, 302 MB of bf16
         X = synthetic.lowrank_batch(B, n, m, base_seed=7600, dtype=torch.bfloat16, device=dev)
         fn = lambda: d3.gram_ns(X, ABC, RESTARTS, compute=torch.float16)  # noqa: E731
+    elif args.case == "moe_w2_cols":
+        B, m, n = 1024, 2048, 768  # the MoE w2 matrices in their stored layout, column selection
+        W = synthetic.gaussian((B, m, n), seed=7700, std=0.02, device=dev)
+        M = torch.zeros((B, m, n), dtype=torch.float32, device=dev)
+        G = synthetic.lowrank_batch(B, m, n, base_seed=7800, dtype=torch.bfloat16, device=dev)
+        fn = lambda: d3.step_cols(W, M, G, f=(1, 8), mu=MU, eta=ETA, abc=ABC, restart_after=RESTARTS)  # noqa: E731
     elif args.case == "fp32":
         X = synthetic.gaussian((256, 1024), seed=0, device="cpu").to(dev)
         fn = lambda: d3.gram_ns(X, ABC, (2,), compute=torch.float32)  # noqa: E731
