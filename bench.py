@@ -45,6 +45,10 @@ MEGABATCHES = [(128, 4096, 4096), (96, 4096, 11008)]  # (batch, n, m): attention
 F = (1, 4)
 MU, ETA = 0.95, 0.01
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Pass C with the decay carried: reads M[S,:] (fp32) and writes X_S (fp16); M[S,:] is not written.
+GATHER_BYTES = 6.0
+DECAY_NOTE = ("M[S,:] <- mu M[S,:] of each step is applied by the next step's momentum pass "
+              "(dion3_step_carry: same fp32 roundings, bit-identical state; pass C skips its write of M[S,:])")
 WORKLOAD = ("dion3_step f=1/4 on 7B dense shapes: megabatches 128x4096x4096 + 96x4096x11008 "
             "(k=1024, alpha'=4 and 10.75), T=5 Jordan triple, restarts after 2 and 4, mu=0.95, eta=0.01, l1 "
             "selection, fp16 Gram iterates, W/M fp32, G bf16")
@@ -172,6 +176,16 @@ def step_inputs(torch, synthetic, dev, rank: int):
     return mbs
 
 
+def carried_step(d3, x, slot, ws, status, events=None, f=F):
+    """One step of megabatch x; its decay of M[S,:] is left to the next call (x["carried"])."""
+    import torch
+
+    d3.step(x["W"], x["M"], x["Gs"][slot], f=f, mu=MU, eta=ETA, norm_p=1, abc=ABC, restart_after=RESTARTS,
+            compute=torch.float16, sel_out=x["sel"], workspace=ws, status=status, events=events,
+            carry=(x["sel"], MU) if x.get("carried") else None, defer=True)
+    x["carried"] = True
+
+
 # ----------------------------------------------------------------------------- ours
 def run_ours(args):
     import torch
@@ -210,9 +224,7 @@ def run_ours(args):
 
     def one_step(s_idx, events=None):
         for gi, x in enumerate(mbs):
-            d3.step(x["W"], x["M"], x["Gs"][s_idx % 2], f=F, mu=MU, eta=ETA, norm_p=1, abc=ABC,
-                    restart_after=RESTARTS, compute=torch.float16, sel_out=x["sel"], workspace=ws, status=status,
-                    events=None if events is None else events[gi])
+            carried_step(d3, x, s_idx % 2, ws, status, None if events is None else events[gi])
 
     for s in range(args.warmup):
         one_step(s)
@@ -258,7 +270,7 @@ def run_ours(args):
     hbm = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
     tc_sus = float(peaks.get("bf16_tflops_sustained", PEAKS_FALLBACK["bf16_tflops_sustained"]))
     bytesA = sum(10.0 * x["B"] * x["n"] * x["m"] for x in mbs)
-    bytesC = sum(10.0 * x["B"] * k_rows(x["n"]) * x["m"] for x in mbs)
+    bytesC = sum(GATHER_BYTES * x["B"] * k_rows(x["n"]) * x["m"] for x in mbs)
     flops = sum(float(x["B"] * gram_flops(k_rows(x["n"]), x["m"])) for x in mbs)
     ph = {n: sum(pm[i] for pm in per_mb) for i, n in enumerate(names)}
     phases = {
@@ -274,9 +286,9 @@ def run_ours(args):
         "per_megabatch_ms": [{"shape": f"{x['B']}x{x['n']}x{x['m']}", "ms": sum(pm)} for x, pm in zip(mbs, per_mb)],
     }
     dominant = max(names, key=lambda n: ph[n])
-    launches_per_mb = d3.step_launch_count(T_ITERS, RESTARTS, k_rows(MEGABATCHES[0][1]))
+    launches_per_mb = d3.step_launch_count(T_ITERS, RESTARTS, k_rows(MEGABATCHES[0][1]), carry=True)
     if dominant == "gram_ns_products":
-        n_launch = len(mbs) * (launches_per_mb - 3)
+        n_launch = sum(d3.gram_core_launch_count(T_ITERS, RESTARTS, k_rows(x["n"])) for x in mbs)
         achieved = flops / ph[dominant] / 1e9
         roof = {"kernel": "tc_gemm_kernel (all tcgen05 GEMM launches of the Gram-NS chain)", "bound": "tensor",
                 "achieved": achieved, "peak": tc_sus, "unit": "TFLOP/s", "frac": achieved / tc_sus,
@@ -306,6 +318,7 @@ def run_ours(args):
         "config": {"workload": WORKLOAD, "megabatches": [f"{b}x{n}x{m}" for b, n, m in MEGABATCHES],
                    "l2": "inputs larger than L2 (about 65 GB touched per step)", "state": "W, M fp32; G bf16",
                    "gram_iterates": "float16 (the paper's precision), fp32 accumulation",
+                   "error_feedback": DECAY_NOTE,
                    "parallelism": f"replica per GPU x{world} (independent megabatches, no collective)"},
         "roofline": roof,
         "phases": phases,
@@ -383,8 +396,7 @@ def run_e2e(torch, d3, mbs, ws, status, args, dev, dist):
     def enqueue_step(t):
         comp.wait_event(copied[t])
         for x, hs in zip(mbs, host_sel):
-            d3.step(x["W"], x["M"], x["Gs"][t % 2], f=F, mu=MU, eta=ETA, norm_p=1, abc=ABC, restart_after=RESTARTS,
-                    compute=torch.float16, sel_out=x["sel"], workspace=ws, status=status)
+            carried_step(d3, x, t % 2, ws, status)
             hs.copy_(x["sel"], non_blocking=True)
         computed[t].record(comp)
 
@@ -489,7 +501,8 @@ def bench_moe_step(torch, d3, synthetic, dev, peaks, peaks_kind):
 
     def fn(events=None):
         d3.step(W, M, Gs[state["s"] % 2], f=fk, mu=MU, eta=ETA, norm_p=1, abc=ABC, restart_after=RESTARTS,
-                compute=torch.float16, sel_out=sel, workspace=ws, events=events)
+                compute=torch.float16, sel_out=sel, workspace=ws, events=events,
+                carry=(sel, MU) if state["s"] > 0 else None, defer=True)
         state["s"] += 1
 
     for _ in range(3):
@@ -501,8 +514,9 @@ def bench_moe_step(torch, d3, synthetic, dev, peaks, peaks_kind):
     ph = [evs[i].elapsed_time(evs[i + 1]) for i in range(4)]
     hbm = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
     bytes_a = 10.0 * B * n * m
-    bytes_c = 10.0 * B * k * m
-    out = {"workload": "dion3_step f=1/8 on 3072 x 768x2048 (MoE experts), T=5 Jordan, restarts 2,4, fp16 iterates",
+    bytes_c = GATHER_BYTES * B * k * m
+    out = {"workload": "dion3_step f=1/8 on 3072 x 768x2048 (MoE experts), T=5 Jordan, restarts 2,4, fp16 iterates, "
+                       "decay of M[S] carried",
            "ms": ms, "phases_ms": {"momentum_keys": ph[0], "select": ph[1], "gather": ph[2], "gram_ns_products": ph[3]},
            "momentum_frac_hbm": bytes_a / ph[0] / 1e6 / hbm,
            "hbm_floor_ms": (bytes_a + bytes_c) / hbm / 1e6,
@@ -619,8 +633,10 @@ def oracle_step_ms(samples) -> float:
 
 def cpu_baseline_and_parity(torch, d3, dev, sample0):
     """The oracle's Dion3 step on matrix 0 of each megabatch (its first-step inputs, as generated
-    on the device), timed on the host cores and scaled by the megabatch sizes; and the same step
-    through the C ABI on those inputs (batch 1), compared with the oracle's result."""
+    on the device), timed on the host cores and scaled by the megabatch sizes; and two steps (the
+    second with the same G) through the C ABI as the timed loop runs them (batch 1, decay of
+    M[S,:] carried into the second step's momentum pass and applied at the end), compared with
+    the oracle's two plain steps."""
     import numpy as np
 
     import oracle
@@ -634,26 +650,34 @@ def cpu_baseline_and_parity(torch, d3, dev, sample0):
         W1, M1, S, _ = oracle.dion3_step(W0, M0, G0, F[0], F[1], mu=MU, eta=ETA, norm_p=1, abc=ABC,
                                          restart_after=RESTARTS)
         total += (time.perf_counter() - t0) * B
+        W2, M2, S2, _ = oracle.dion3_step(W1, M1, G0, F[0], F[1], mu=MU, eta=ETA, norm_p=1, abc=ABC,
+                                          restart_after=RESTARTS)
         Wd = torch.from_numpy(W0).to(dev).unsqueeze(0).contiguous()
         Md = torch.zeros((1, n, m), dtype=torch.float32, device=dev)
         Gd = torch.from_numpy(G0).to(device=dev, dtype=torch.bfloat16).unsqueeze(0).contiguous()
         status = torch.zeros(1, dtype=torch.int32, device=dev)
-        sel = d3.step(Wd, Md, Gd, f=F, mu=MU, eta=ETA, norm_p=1, abc=ABC, restart_after=RESTARTS,
-                      compute=torch.float16, status=status)
+        x = {"W": Wd, "M": Md, "Gs": [Gd, Gd], "sel": torch.empty((1, k_rows(n)), dtype=torch.int32, device=dev)}
+        carried_step(d3, x, 0, None, status)
+        sel1 = x["sel"][0].cpu().numpy()
+        Wd1 = Wd[0].double().cpu().numpy()
+        carried_step(d3, x, 1, None, status)
+        d3.decay_rows(Md, x["sel"], MU)
         torch.cuda.synchronize()
-        dW = Wd[0].double().cpu().numpy() - W0
-        ref = W1 - W0
-        checks.append({"shape": f"{n}x{m}", "rows_selected_equal": bool(np.array_equal(sel[0].cpu().numpy(), S)),
-                       "M_bit_exact": bool(np.array_equal(Md[0].cpu().numpy().view(np.uint32), M1.view(np.uint32))),
-                       "dW_rel_frob": float(np.linalg.norm(dW - ref) / np.linalg.norm(ref)),
+        rel = lambda got, ref: float(np.linalg.norm(got - ref) / np.linalg.norm(ref))  # noqa: E731
+        checks.append({"shape": f"{n}x{m}",
+                       "rows_selected_equal": bool(np.array_equal(sel1, S) and
+                                                   np.array_equal(x["sel"][0].cpu().numpy(), S2)),
+                       "M_bit_exact": bool(np.array_equal(Md[0].cpu().numpy().view(np.uint32), M2.view(np.uint32))),
+                       "dW_rel_frob": max(rel(Wd1 - W0, W1 - W0), rel(Wd[0].double().cpu().numpy() - Wd1, W2 - W1)),
                        "device_status": int(status.item())})
-        del Wd, Md, Gd
+        del Wd, Md, Gd, x
     base = {"value": total * 1e3, "unit": "ms per megabatch step (both 7B shape groups)",
             "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
             "sample": "one oracle Dion3 step (float64, exact keys) on matrix 0 of each megabatch "
                       "(4096x4096 and 4096x11008, first-step inputs, M=0), scaled by the megabatch sizes 128 and 96"}
-    parity = {"against": "the oracle's step on matrix 0 of each megabatch (the cpu_baseline sample), same inputs, "
-                         "run through the C ABI with batch 1",
+    parity = {"against": "two oracle steps on matrix 0 of each megabatch (the cpu_baseline sample's inputs, G "
+                         "used twice), run through the C ABI with batch 1 as the timed loop runs them (carried "
+                         "decay, applied at the end); rows of both steps, M after both, worst dW of the two",
               "tolerance": {"rows": "bit-exact", "M": "bit-exact", "dW_rel_frob": 3e-2}, "checks": checks}
     return base, parity
 
@@ -712,13 +736,15 @@ def run_case(args):
         W = synthetic.gaussian((B, n, m), seed=7100, std=0.02, device=dev)
         M = torch.zeros((B, n, m), dtype=torch.float32, device=dev)
         G = synthetic.lowrank_batch(B, n, m, base_seed=7200, dtype=torch.bfloat16, device=dev)
-        fn = lambda: d3.step(W, M, G, f=F, mu=MU, eta=ETA, abc=ABC, restart_after=RESTARTS)  # noqa: E731
+        x = {"W": W, "M": M, "Gs": [G], "sel": torch.empty((B, k_rows(n)), dtype=torch.int32, device=dev)}
+        fn = lambda: carried_step(d3, x, 0, None, None)  # noqa: E731
     elif args.case == "moe":
         B, n, m = 3072, 768, 2048  # the MoE megabatch at full size (launch-list captures only)
         W = synthetic.gaussian((B, n, m), seed=7400, std=0.02, device=dev)
         M = torch.zeros((B, n, m), dtype=torch.float32, device=dev)
         G = synthetic.lowrank_batch(B, n, m, base_seed=7500, dtype=torch.bfloat16, device=dev)
-        fn = lambda: d3.step(W, M, G, f=(1, 8), mu=MU, eta=ETA, abc=ABC, restart_after=RESTARTS)  # noqa: E731
+        x = {"W": W, "M": M, "Gs": [G], "sel": torch.empty((B, 96), dtype=torch.int32, device=dev)}
+        fn = lambda: carried_step(d3, x, 0, None, None, f=(1, 8))  # noqa: E731
     elif args.case == "moe_gram":
         B, n, m = 768, 96, 2048  # a quarter of the MoE megabatch's selected rows, 302 MB of bf16
         X = synthetic.lowrank_batch(B, n, m, base_seed=7600, dtype=torch.bfloat16, device=dev)

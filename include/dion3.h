@@ -297,6 +297,51 @@ int dion3_step_dev(int batch, int n, int m,
                    int* status_dev, void* stream);
 
 /*
+ * dion3_step_carry -- dion3_step_timed whose error-feedback decay of M[S,:] moves into the next
+ * call's momentum pass.  [D3] "method details" Algorithm 4 and prerequisite "error feedback":
+ * the decay M[S,:] <- mu M[S,:] ends one step and the next step's first operation is
+ * M <- M + G, so it can be applied as M_i <- (mu M_i) + G_i by the pass that reads and writes
+ * every row of M anyway, saving the gather pass its write of M[S,:] (4 of its 10 bytes per
+ * selected element).  Each product is rounded to fp32 before the sum, so the results are
+ * bit-identical to dion3_step's.  (Not a step of the pages: a reordering of theirs.)
+ *   carry_rows : NULL, or int32 [batch][k] device rows (same k as this call) whose decay by
+ *                carry_mu an earlier call left pending -- that call's sel_out.  They are
+ *                applied before M <- M + G.  Entries outside [0, n) (the -1 of a failed
+ *                selection) are skipped; a row listed more than once is scaled once.  4-byte
+ *                aligned.  It may be the same buffer as sel_out (it is read before the new S
+ *                is written), except with norm_p = DION3_SELECT_GIVEN, where sel_out holds
+ *                the new S on entry: that aliasing is EINVAL.
+ *   carry_mu   : the factor of the pending decay (that call's mu); must be finite.
+ *   defer      : nonzero leaves this call's own decay of M[S,:] by mu pending: on return
+ *                M[S,:] holds M + G, and the caller passes (sel_out, mu) as the next call's
+ *                (carry_rows, carry_mu) or applies it with dion3_decay_rows.  Zero applies it
+ *                as dion3_step does.
+ *   Workspace: dion3_step_workspace_bytes.  Everything else as dion3_step_timed (events may
+ *   be NULL with n_events = 0).  One extra launch (the per-row flags) when carry_rows is set.
+ *   Errors: as dion3_step; EINVAL for a non-finite carry_mu or the aliasing above, EALIGN
+ *   for a misaligned carry_rows.
+ */
+int dion3_step_carry(int batch, int n, int m,
+                     float* W, float* M, const void* G, int g_dtype,
+                     int f_num, int f_den, float mu, float eta, float wd, int norm_p,
+                     int T, const float* abc, const int* restart_after, int n_restart, float eps,
+                     int compute_dtype, int32_t* sel_out,
+                     const int32_t* carry_rows, float carry_mu, int defer,
+                     void* workspace, size_t workspace_bytes,
+                     int* status_dev, void* stream, void* const* events, int n_events);
+
+/*
+ * dion3_decay_rows -- applies a decay that dion3_step_carry left pending:
+ *   M[b][rows[b][j]][:] <- mu * M[b][rows[b][j]][:]  (fp32, one rounding)
+ * for j < k and rows in [0, n); other entries are skipped.  List each row once (as sel_out
+ * does): a repeated row is scaled once per listing.
+ *   M    : fp32 [batch][n][m] contiguous, 4-byte aligned.  rows : int32 [batch][k], 4-byte aligned.
+ *   Errors: EINVAL (negative sizes, k > n, non-finite mu, NULL pointers with work to do),
+ *   EALIGN, ECUDA.  Nothing to do (batch, k or m zero) returns DION3_OK.
+ */
+int dion3_decay_rows(int batch, int n, int m, float* M, const int32_t* rows, int k, float mu, void* stream);
+
+/*
  * dion3_gram_ns_noalloc -- dion3_gram_ns for callers that cannot allocate device memory
  * (no counterpart in the paper).  Same arguments and results as dion3_gram_ns, minus the
  * workspace: the scratch comes from an array of DION3_NOALLOC_SCRATCH_BYTES compiled into the

@@ -60,6 +60,11 @@ SIGNATURES = {
     "dion3_step_dev": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_p, _c_int,
                                 _c_int, _c_int, ctypes.POINTER(_c_f), ctypes.POINTER(_c_int), _c_int, _c_f, _c_int,
                                 _c_p, _c_p, _c_sz, _c_p, _c_p]),
+    "dion3_step_carry": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_f, _c_f,
+                                  _c_f, _c_int, _c_int, ctypes.POINTER(_c_f), ctypes.POINTER(_c_int), _c_int, _c_f,
+                                  _c_int, _c_p, _c_p, _c_f, _c_int, _c_p, _c_sz, _c_p, _c_p, ctypes.POINTER(_c_p),
+                                  _c_int]),
+    "dion3_decay_rows": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_p, _c_int, _c_f, _c_p]),
     "dion3_gram_ns_noalloc": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_i64, _c_i64, _c_int, _c_p, _c_i64, _c_i64,
                                        _c_int, _c_int, ctypes.POINTER(_c_f), ctypes.POINTER(_c_int), _c_int, _c_f,
                                        _c_int, _c_p, _c_p]),
@@ -266,7 +271,7 @@ def step(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, f=(1, 4), mu: float 
          wd: float = 0.0, norm_p: int = 1, abc=None, restart_after=(2,), eps: float = 1e-7, compute=torch.float16,
          sel_out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
          status: torch.Tensor | None = None, events=None, hyper: torch.Tensor | None = None,
-         decay: bool = False, rows: torch.Tensor | None = None) -> torch.Tensor:
+         decay: bool = False, rows: torch.Tensor | None = None, carry=None, defer: bool = False) -> torch.Tensor:
     """One Dion3 step on [batch, n, m] (or [n, m]) contiguous W, M (fp32) and G; returns the selected rows.
 
     ``events``: optional list of up to five recorded-once ``torch.cuda.Event`` objects, recorded
@@ -277,7 +282,14 @@ def step(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, f=(1, 4), mu: float 
     ``rows``: optional caller-chosen row set S, int32 [batch, k] (or [k]) with strictly ascending
     rows per matrix (e.g. a sorted random subset); no keys are computed (``norm_p`` is ignored).
     A matrix whose rows break the rule is left unselected and flags DION3_DEV_SELECT.
+    ``defer``: leave this step's decay of M[S,:] by ``mu`` pending (M[S,:] keeps M + G) and
+    pass ``carry=(sel, mu)`` -- the returned rows and this mu -- to the next call, whose momentum
+    pass applies it (dion3_step_carry in include/dion3.h); ``decay_rows`` applies it on its own.
+    The state that results is bit-identical to that of plain steps.
     """
+    carrying = carry is not None or defer
+    if carrying and hyper is not None:
+        raise ValueError("carry/defer take host hyperparameters (hyper must be None)")
     for t, name in ((W, "W"), (M, "M"), (G, "G")):
         _cuda(t, name)
         if not t.is_contiguous():
@@ -301,6 +313,12 @@ def step(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, f=(1, 4), mu: float 
         if rows.data_ptr() != sel_out.data_ptr():
             sel_out.copy_(rows)
         norm_p = SELECT_GIVEN
+    carry_rows, carry_mu = None, 1.0
+    if carry is not None:
+        carry_rows, carry_mu = carry
+        _cuda(carry_rows, "carry rows")
+        if carry_rows.dtype != torch.int32 or tuple(carry_rows.shape) != shape or not carry_rows.is_contiguous():
+            raise ValueError(f"carry rows must be contiguous int32 of shape {shape}")
     T, flat, rarr, nr = _abc_arrays(abc, restart_after)
     need = workspace_bytes_step(batch, n, m, f_num, f_den, norm_p, compute, nr)
     if workspace is None:
@@ -316,6 +334,15 @@ def step(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, f=(1, 4), mu: float 
                                   _ptr(sel_out), _ptr(workspace), workspace.numel(), _ptr(status),
                                   _stream_ptr(M.device))
         _check(rc, "dion3_step_dev")
+    elif carrying:
+        evs = list(events) if events is not None else []
+        handles = (_c_p * max(len(evs), 1))(*[ctypes.c_void_p(e.cuda_event) for e in evs])
+        rc = lib().dion3_step_carry(batch, n, m, _ptr(W), _ptr(M), _ptr(G), _dt(G), f_num, f_den, float(mu),
+                                    float(eta), float(wd), norm_p, T, flat, rarr, nr, float(eps),
+                                    _dtype_code(compute), _ptr(sel_out), _ptr(carry_rows), float(carry_mu),
+                                    int(bool(defer)), _ptr(workspace), workspace.numel(), _ptr(status),
+                                    _stream_ptr(M.device), handles, len(evs))
+        _check(rc, "dion3_step_carry")
     elif events is None:
         rc = lib().dion3_step(batch, n, m, _ptr(W), _ptr(M), _ptr(G), _dt(G), f_num, f_den, float(mu), float(eta),
                               float(wd), norm_p, T, flat, rarr, nr, float(eps), _dtype_code(compute), _ptr(sel_out),
@@ -329,6 +356,23 @@ def step(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, f=(1, 4), mu: float 
                                     _ptr(status), _stream_ptr(M.device), handles, len(events))
         _check(rc, "dion3_step_timed")
     return sel_out
+
+
+def decay_rows(M: torch.Tensor, rows: torch.Tensor, mu: float) -> None:
+    """M[b, rows[b, j], :] *= mu (fp32, one rounding): applies a decay that ``step(defer=True)``
+    left pending.  M is [batch, n, m] (or [n, m]) contiguous fp32, rows int32 [batch, k] (or [k])."""
+    _cuda(M, "M")
+    _cuda(rows, "rows")
+    if M.dtype != torch.float32 or not M.is_contiguous():
+        raise ValueError("M must be contiguous fp32")
+    if rows.dtype != torch.int32 or not rows.is_contiguous() or rows.dim() != M.dim() - 1:
+        raise ValueError("rows must be contiguous int32 with one dimension fewer than M")
+    batch, n, m, _, _ = _layout(M)
+    k = rows.shape[-1]
+    if M.dim() == 3 and rows.shape[0] != batch:
+        raise ValueError("rows must have one row list per matrix")
+    rc = lib().dion3_decay_rows(batch, n, m, _ptr(M), _ptr(rows), k, float(mu), _stream_ptr(M.device))
+    _check(rc, "dion3_decay_rows")
 
 
 def workspace_bytes_step_cols(batch: int, m: int, n: int, f_num: int, f_den: int, norm_p: int, compute,
@@ -411,10 +455,11 @@ def gram_core_launch_count(T: int, restart_after=(), n: int | None = None, compu
     return count + 1
 
 
-def step_launch_count(T: int, restart_after=(), k: int | None = None, compute=torch.float16) -> int:
+def step_launch_count(T: int, restart_after=(), k: int | None = None, compute=torch.float16,
+                      carry: bool = False) -> int:
     """Kernel launches of one dion3_step call (k selected rows): momentum pass, selection, gather,
-    product chain."""
-    return 3 + gram_core_launch_count(T, restart_after, k, compute)
+    product chain; with a carried decay, the per-row flag pass before the momentum pass."""
+    return 3 + int(bool(carry)) + gram_core_launch_count(T, restart_after, k, compute)
 
 
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024  # DION3_NOALLOC_SCRATCH_BYTES in include/dion3.h

@@ -88,7 +88,7 @@ NsLayout ns_layout(int batch, int n, int m, int cdt) {
 }
 
 struct StepLayout {
-  size_t key_lo, key_hi, exact, rowsq, scale, xs;
+  size_t key_lo, key_hi, exact, rowsq, scale, xs, carry;
   size_t part_s, part_q, obuf;  // column selection: chunk sums of the column keys, and O
   int nchunk;
   CoreLayout core;
@@ -105,6 +105,7 @@ StepLayout step_layout(int batch, int n, int m, int k, int norm_p, int cdt, int 
   L.rowsq = cv.take(sizeof(float) * static_cast<size_t>(batch) * n);
   L.scale = cv.take(sizeof(float) * batch);
   L.xs = cv.take(static_cast<size_t>(batch) * k * round_up(m, 8) * dtype_size(cdt));
+  L.carry = cols ? 0 : cv.take(static_cast<size_t>(batch) * n);  // per-row flags of a carried decay
   if (cols) {
     L.nchunk = (m + STEP_COL_CHUNK - 1) / STEP_COL_CHUNK;
     L.part_s = cv.take(sizeof(float) * static_cast<size_t>(batch) * L.nchunk * n);
@@ -566,8 +567,16 @@ int step_impl(int batch, int n, int m, float* W, float* M, const void* G, int g_
               float mu, float eta, float wd, const float* hyper_dev, bool decay, int norm_p, int T, const float* abc,
               const int* restart_after, int n_restart, float eps, int compute_dtype, int32_t* sel_out,
               void* workspace, size_t workspace_bytes, int* status_dev, void* stream, void* const* events,
-              int n_events, bool cols = false) {
+              int n_events, bool cols = false, const int32_t* carry_rows = nullptr, float carry_mu = 1.f,
+              bool defer = false) {
   if (n_events < 0 || (n_events > 0 && events == nullptr)) return DION3_EINVAL;
+  if (cols && (carry_rows != nullptr || defer)) return DION3_EUNSUPPORTED;
+  if (carry_rows != nullptr) {
+    if (!std::isfinite(carry_mu)) return DION3_EINVAL;
+    // A caller-chosen S is read from sel_out: a carried list there would be the new S.
+    if (norm_p == DION3_SELECT_GIVEN && carry_rows == sel_out) return DION3_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(carry_rows) & 3u) != 0) return DION3_EALIGN;
+  }
   if (batch < 0 || n < 0 || m < 0) return DION3_EINVAL;
   if (!dtype_valid(g_dtype) || !dtype_valid(compute_dtype)) return DION3_EINVAL;
   if (norm_p != DION3_SELECT_GIVEN && norm_p != 1 && norm_p != 2) return DION3_EINVAL;
@@ -626,6 +635,11 @@ int step_impl(int batch, int n, int m, float* W, float* M, const void* G, int g_
     sa.part_s = reinterpret_cast<float*>(ws + L.part_s);
     sa.part_q = reinterpret_cast<float*>(ws + L.part_q);
     sa.nchunk = L.nchunk;
+  } else {
+    sa.carry_rows = carry_rows;
+    sa.carry_flag = reinterpret_cast<uint8_t*>(ws + L.carry);
+    sa.carry_mu = carry_mu;
+    sa.defer = defer;
   }
 
   // Phase boundaries for the caller's timing events (0: start ... 4: end).
@@ -722,6 +736,26 @@ int dion3_step_dev(int batch, int n, int m, float* W, float* M, const void* G, i
   return step_impl(batch, n, m, W, M, G, g_dtype, f_num, f_den, 0.f, 0.f, 0.f, hyper_dev, decay != 0, norm_p, T,
                    abc, restart_after, n_restart, eps, compute_dtype, sel_out, workspace, workspace_bytes, status_dev,
                    stream, nullptr, 0);
+}
+
+int dion3_step_carry(int batch, int n, int m, float* W, float* M, const void* G, int g_dtype, int f_num, int f_den,
+                     float mu, float eta, float wd, int norm_p, int T, const float* abc, const int* restart_after,
+                     int n_restart, float eps, int compute_dtype, int32_t* sel_out, const int32_t* carry_rows,
+                     float carry_mu, int defer, void* workspace, size_t workspace_bytes, int* status_dev,
+                     void* stream, void* const* events, int n_events) {
+  return step_impl(batch, n, m, W, M, G, g_dtype, f_num, f_den, mu, eta, wd, nullptr, false, norm_p, T, abc,
+                   restart_after, n_restart, eps, compute_dtype, sel_out, workspace, workspace_bytes, status_dev,
+                   stream, events, n_events, false, carry_rows, carry_mu, defer != 0);
+}
+
+int dion3_decay_rows(int batch, int n, int m, float* M, const int32_t* rows, int k, float mu, void* stream) {
+  if (batch < 0 || n < 0 || m < 0 || k < 0 || k > n) return DION3_EINVAL;
+  if (!std::isfinite(mu)) return DION3_EINVAL;
+  if (batch == 0 || k == 0 || m == 0) return DION3_OK;
+  if (M == nullptr || rows == nullptr) return DION3_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(M) & 3u) != 0 || (reinterpret_cast<uintptr_t>(rows) & 3u) != 0)
+    return DION3_EALIGN;
+  return step_decay_rows(batch, n, m, k, M, rows, mu, static_cast<cudaStream_t>(stream));
 }
 
 int dion3_selftest_watchdog(long long spin_limit_cycles, int* status_dev, void* stream) {

@@ -122,6 +122,14 @@ struct StepArgs {
   float* part_s = nullptr;
   float* part_q = nullptr;
   int nchunk = 0;
+  // Carried decay.  carry_rows ([batch][k], or null): rows whose decay by carry_mu an earlier
+  // step left pending; pass A first turns them into per-row flags (carry_flag, [batch][n]) and
+  // scales those rows by carry_mu before adding G.  defer: pass C leaves this step's decay of
+  // M[S,:] pending instead of storing mu M[S,:].
+  const int32_t* carry_rows = nullptr;
+  uint8_t* carry_flag = nullptr;
+  float carry_mu = 1.f;
+  bool defer = false;
 };
 int step_momentum_keys(const StepArgs& a, cudaStream_t s);
 int step_select(const StepArgs& a, cudaStream_t s);
@@ -135,6 +143,8 @@ int step_scatter_cols(const StepArgs& a, const void* O, int64_t ldo, float alpha
                       double eta_scale, cudaStream_t s);
 constexpr int STEP_COL_CHUNK = 256;  // rows per partial sum of a column key
 int step_exact_limbs(int norm_p);
+// M[b][rows[b][j]][:] <- mu M[b][rows[b][j]][:] for the listed rows in [0, n).
+int step_decay_rows(int batch, int n, int m, int k, float* M, const int32_t* rows, float mu, cudaStream_t s);
 
 // Watchdog self-test kernel (gemm_tc.cu).
 int selftest_watchdog(long long spin_limit, int* status, cudaStream_t s);

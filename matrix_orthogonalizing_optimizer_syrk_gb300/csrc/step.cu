@@ -75,6 +75,8 @@ struct AArgs {
   float* key_hi;
   float* rowsq;
   int* status;
+  const uint8_t* carry;  // [rows]: nonzero where an earlier step's decay of the row is pending
+  float carry_mu;
 };
 
 // ------------------------------------------------------------------------------ pass A
@@ -95,6 +97,10 @@ __global__ void __launch_bounds__(256) momentum_keys_kernel(const AArgs a) {
     float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
     float q2[4] = {0.f, 0.f, 0.f, 0.f};  // sums of squares for the Frobenius prescale
     bool bad = false;
+    // A pending decay is applied first, rounded to fp32 on its own, so the row ends exactly as
+    // if the earlier step had stored mu M and this pass then added G.
+    const bool cr = a.carry != nullptr && a.carry[row] != 0;
+    const float cm = a.carry_mu;
     if constexpr (VEC) {
       for (int j = lane * 8; j < m; j += 256) {
         float g[8];
@@ -102,6 +108,10 @@ __global__ void __launch_bounds__(256) momentum_keys_kernel(const AArgs a) {
         float4* m4 = reinterpret_cast<float4*>(Mr + j);
         float4 ma = m4[0], mb = m4[1];
         float x[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+        if (cr) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) x[q] = __fmul_rn(cm, x[q]);
+        }
 #pragma unroll
         for (int q = 0; q < 8; ++q) x[q] = __fadd_rn(x[q], g[q]);
         m4[0] = make_float4(x[0], x[1], x[2], x[3]);
@@ -129,7 +139,8 @@ __global__ void __launch_bounds__(256) momentum_keys_kernel(const AArgs a) {
       }
     } else {
       for (int j = lane; j < m; j += 32) {
-        const float x = __fadd_rn(Mr[j], gval<TG>(Gr[j]));
+        const float mv = cr ? __fmul_rn(cm, Mr[j]) : Mr[j];
+        const float x = __fadd_rn(mv, gval<TG>(Gr[j]));
         Mr[j] = x;
         q2[0] = fmaf(x, x, q2[0]);
         if (a.decay) Wr[j] = __fmul_rn(Wr[j], w_decay);
@@ -477,7 +488,8 @@ __device__ __forceinline__ __nv_bfloat16 cvt_out<__nv_bfloat16>(float v) { retur
 template <>
 __device__ __forceinline__ __half cvt_out<__half>(float v) { return __float2half_rn(v); }
 
-template <typename TC, bool VEC>
+// WRITE_M = false leaves M[S,:] as it is: its decay is carried to a later pass.
+template <typename TC, bool VEC, bool WRITE_M>
 __global__ void __launch_bounds__(256) gather_kernel(const CArgs a) {
   const int lane = threadIdx.x & 31;
   const long long w0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -503,8 +515,9 @@ __global__ void __launch_bounds__(256) gather_kernel(const CArgs a) {
         } else {
           *reinterpret_cast<float4*>(dst + c) = make_float4(x.x * f, x.y * f, x.z * f, x.w * f);
         }
-        *reinterpret_cast<float4*>(src + c) =
-            make_float4(__fmul_rn(mu, x.x), __fmul_rn(mu, x.y), __fmul_rn(mu, x.z), __fmul_rn(mu, x.w));
+        if constexpr (WRITE_M)
+          *reinterpret_cast<float4*>(src + c) =
+              make_float4(__fmul_rn(mu, x.x), __fmul_rn(mu, x.y), __fmul_rn(mu, x.z), __fmul_rn(mu, x.w));
       };
       int c = lane * 4;
       for (; c + 384 < a.m; c += 512) {
@@ -519,7 +532,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const CArgs a) {
       for (int c = lane; c < a.m; c += 32) {
         const float x = src[c];
         dst[c] = cvt_out<TC>(x * f);
-        src[c] = __fmul_rn(mu, x);
+        if constexpr (WRITE_M) src[c] = __fmul_rn(mu, x);
       }
     }
   }
@@ -543,16 +556,60 @@ int launch_a_p(const AArgs& a, int norm_p, bool vec, cudaStream_t s) {
 }
 
 template <typename TC>
-int launch_c(const CArgs& c, bool vec, cudaStream_t s) {
+int launch_c(const CArgs& c, bool vec, bool write_m, cudaStream_t s) {
   long long blocks = (c.rows + 7) / 8;
   const long long cap = static_cast<long long>(sm_count()) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) return DION3_OK;
-  if (vec)
-    gather_kernel<TC, true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(c);
+  const unsigned g = static_cast<unsigned>(blocks);
+  if (vec && write_m)
+    gather_kernel<TC, true, true><<<g, 256, 0, s>>>(c);
+  else if (vec)
+    gather_kernel<TC, true, false><<<g, 256, 0, s>>>(c);
+  else if (write_m)
+    gather_kernel<TC, false, true><<<g, 256, 0, s>>>(c);
   else
-    gather_kernel<TC, false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(c);
+    gather_kernel<TC, false, false><<<g, 256, 0, s>>>(c);
   return cudaGetLastError() == cudaSuccess ? DION3_OK : DION3_ECUDA;
+}
+
+// Carried decay, flag pass: flag[b][i] = 1 for the listed rows of matrix b, 0 elsewhere.  One CTA
+// per matrix; entries outside [0, n) (the -1 of a failed selection) list nothing.
+__global__ void __launch_bounds__(256) carry_flags_kernel(int n, int k, const int32_t* rows, uint8_t* flag) {
+  const int b = blockIdx.x;
+  uint8_t* f = flag + static_cast<long long>(b) * n;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) f[i] = 0;
+  __syncthreads();
+  const int32_t* r = rows + static_cast<long long>(b) * k;
+  for (int j = threadIdx.x; j < k; j += blockDim.x) {
+    const int i = r[j];
+    if (i >= 0 && i < n) f[i] = 1;
+  }
+}
+
+// Explicit decay: M[b][rows[b][j]][:] <- mu M[...] (one fp32 rounding), one warp per listed row;
+// entries outside [0, n) are skipped.
+template <bool VEC>
+__global__ void __launch_bounds__(256) decay_rows_kernel(int n, int m, int k, long long nrows, float* M,
+                                                         const int32_t* rows, float mu) {
+  const int lane = threadIdx.x & 31;
+  const long long w0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long r = w0; r < nrows; r += nw) {
+    const long long b = r / k;
+    const int i = rows[r];
+    if (i < 0 || i >= n) continue;
+    float* p = M + (b * n + i) * m;
+    if constexpr (VEC) {
+      for (int c = lane * 4; c < m; c += 128) {
+        float4 x = *reinterpret_cast<const float4*>(p + c);
+        x = make_float4(__fmul_rn(mu, x.x), __fmul_rn(mu, x.y), __fmul_rn(mu, x.z), __fmul_rn(mu, x.w));
+        *reinterpret_cast<float4*>(p + c) = x;
+      }
+    } else {
+      for (int c = lane; c < m; c += 32) p[c] = __fmul_rn(mu, p[c]);
+    }
+  }
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -577,7 +634,13 @@ int step_momentum_keys(const StepArgs& s, cudaStream_t st) {
   a.key_hi = s.key_hi;
   a.rowsq = s.rowsq;
   a.status = s.status;
+  a.carry = s.carry_rows != nullptr ? s.carry_flag : nullptr;
+  a.carry_mu = s.carry_mu;
   if (a.rows == 0) return DION3_OK;
+  if (a.carry != nullptr) {
+    carry_flags_kernel<<<s.batch, 256, 0, st>>>(s.n, s.k, s.carry_rows, s.carry_flag);
+    if (cudaGetLastError() != cudaSuccess) return DION3_ECUDA;
+  }
   const bool vec = (s.m % 8 == 0) && aligned16(s.M) && aligned16(s.G) && aligned16(s.W);
   switch (s.g_dtype) {
     case FP32:
@@ -644,12 +707,26 @@ int step_gather(const StepArgs& s, cudaStream_t st) {
   const bool vec = (s.m % 4 == 0) && aligned16(s.M) && (s.ldx % 8 == 0);
   switch (s.cdt) {
     case FP32:
-      return launch_c<float>(c, vec, st);
+      return launch_c<float>(c, vec, !s.defer, st);
     case FP16:
-      return launch_c<__half>(c, vec, st);
+      return launch_c<__half>(c, vec, !s.defer, st);
     default:
-      return launch_c<__nv_bfloat16>(c, vec, st);
+      return launch_c<__nv_bfloat16>(c, vec, !s.defer, st);
   }
+}
+
+int step_decay_rows(int batch, int n, int m, int k, float* M, const int32_t* rows, float mu, cudaStream_t st) {
+  const long long nrows = static_cast<long long>(batch) * k;
+  if (nrows == 0 || m == 0) return DION3_OK;
+  long long blocks = (nrows + 7) / 8;
+  const long long cap = static_cast<long long>(sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  const bool vec = (m % 4 == 0) && aligned16(M);
+  if (vec)
+    decay_rows_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, st>>>(n, m, k, nrows, M, rows, mu);
+  else
+    decay_rows_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, st>>>(n, m, k, nrows, M, rows, mu);
+  return cudaGetLastError() == cudaSuccess ? DION3_OK : DION3_ECUDA;
 }
 
 }  // namespace dion3

@@ -223,3 +223,40 @@ def test_step_cols_validation(L):
     assert call(p=3) == 1
     assert call(batch=70000, wsb=16) == 2
     assert d3.workspace_bytes_step_cols(2, 128, 64, 1, 4, 1, 0, 2) > d3.workspace_bytes_step(2, 64, 128, 1, 4, 1, 0, 2)
+
+
+def test_step_carry_validation(L):
+    """dion3_step_carry rejects a bad carried decay before any launch."""
+    r = (ctypes.c_int * 1)(2)
+    SEL = ctypes.c_void_p(0x20000)
+
+    def call(carry=FAKE, cmu=0.95, defer=1, p=1, sel=SEL, ws=FAKE, wsb=1 << 40, n_events=0):
+        return L.dion3_step_carry(1, 64, 128, FAKE, FAKE, FAKE, 0, 1, 4, 0.95, 0.01, 0.0, p, 5, _abc(5), r, 1,
+                                  1e-7, 0, sel, carry, cmu, defer, ws, wsb, NULL, NULL, None, n_events)
+
+    assert call(cmu=float("nan")) == 1
+    assert call(cmu=float("inf")) == 1
+    assert call(carry=ctypes.c_void_p(0x10002)) == 5      # int32 list not 4-byte aligned
+    assert call(p=0, carry=SEL) == 1                       # S given in sel_out: cannot also be the carried list
+    assert call(p=0, carry=FAKE, ws=NULL) == 3             # a separate carried list is fine with a given S
+    assert call(carry=SEL, ws=NULL) == 3                   # aliasing sel_out is fine with computed keys
+    assert call(carry=NULL, defer=0, ws=NULL) == 3
+    assert call(n_events=-1) == 1
+    assert call(carry=NULL, cmu=float("nan"), wsb=16) == 3  # carry_mu is unused without a list
+
+
+def test_decay_rows_validation(L):
+    assert L.dion3_decay_rows(-1, 8, 8, FAKE, FAKE, 2, 0.9, NULL) == 1
+    assert L.dion3_decay_rows(1, 8, 8, FAKE, FAKE, 9, 0.9, NULL) == 1        # k > n
+    assert L.dion3_decay_rows(1, 8, 8, FAKE, FAKE, 2, float("nan"), NULL) == 1
+    assert L.dion3_decay_rows(1, 8, 8, NULL, FAKE, 2, 0.9, NULL) == 1
+    assert L.dion3_decay_rows(1, 8, 8, FAKE, NULL, 2, 0.9, NULL) == 1
+    assert L.dion3_decay_rows(1, 8, 8, ctypes.c_void_p(0x10002), FAKE, 2, 0.9, NULL) == 5
+    assert L.dion3_decay_rows(1, 8, 8, FAKE, ctypes.c_void_p(0x10001), 2, 0.9, NULL) == 5
+    assert L.dion3_decay_rows(0, 8, 8, NULL, NULL, 2, 0.9, NULL) == 0        # nothing to do
+    assert L.dion3_decay_rows(1, 8, 8, NULL, NULL, 0, 0.9, NULL) == 0
+
+
+def test_carry_adds_one_launch():
+    base = d3.step_launch_count(5, (2, 4), 1024)
+    assert d3.step_launch_count(5, (2, 4), 1024, carry=True) == base + 1
