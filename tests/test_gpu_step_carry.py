@@ -191,3 +191,25 @@ def test_carried_decay_at_megabatch_size():
     d3.decay_rows(Mc, sel, MUS[1])
     torch.cuda.synchronize()
     assert torch.equal(Mp, Mc)
+
+
+def test_last_step_without_defer_needs_no_flush():
+    """A carried chain whose last call takes the carry but does not defer (defer=False) ends with
+    M exactly as after plain steps, with no dion3_decay_rows call."""
+    batch, n, m, f = 2, 96, 512, (1, 4)
+    W = synthetic.gaussian((batch, n, m), seed=40, std=0.02, device=DEV)
+    M = synthetic.gaussian((batch, n, m), seed=41, std=0.01, device=DEV)
+    Wp, Mp, Wc, Mc = W.clone(), M.clone(), W.clone(), M.clone()
+    sel = torch.empty((batch, d3.k_of(n, *f)), dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    carry = None
+    for t, mu in enumerate(MUS[:3]):
+        G = synthetic.lowrank_batch(batch, n, m, base_seed=950 + 1000 * t, dtype=torch.bfloat16, device=DEV)
+        d3.step(Wp, Mp, G, f=f, mu=mu, abc=ABC, restart_after=(2,), status=status)
+        last = t == 2
+        d3.step(Wc, Mc, G, f=f, mu=mu, abc=ABC, restart_after=(2,), status=status, sel_out=sel, carry=carry,
+                defer=not last)
+        carry = (sel, mu)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(Wp, Wc) and torch.equal(Mp, Mc)
