@@ -331,6 +331,30 @@ int dion3_step_carry(int batch, int n, int m,
                      int* status_dev, void* stream, void* const* events, int n_events);
 
 /*
+ * dion3_step_dev_carry -- dion3_step_dev with the carried decay of dion3_step_carry, for a
+ * graph captured once and replayed every step: the carried factor lives on the device.
+ *   carry_rows   : as dion3_step_carry (typically sel_out itself).
+ *   carry_mu_dev : device float, 4-byte aligned; required when carry_rows is set or defer is
+ *                  nonzero.  The momentum pass reads the pending factor from it (when carry_rows
+ *                  is set); with defer, the gather pass then stores this call's mu
+ *                  (hyper_dev[0]) there, so the next replay applies it.  Before the first
+ *                  replay set it to 1.0f (and sel_out to -1 or any rows in range): a factor of
+ *                  1 leaves every row exactly as it is.  The value is not checked for
+ *                  finiteness.
+ *   defer        : as dion3_step_carry.  Everything else as dion3_step_dev.
+ *   Errors: as dion3_step_dev; EINVAL when carry_mu_dev is needed and NULL, EALIGN when it is
+ *   misaligned; the carry_rows rules of dion3_step_carry.
+ */
+int dion3_step_dev_carry(int batch, int n, int m,
+                         float* W, float* M, const void* G, int g_dtype,
+                         int f_num, int f_den, const float* hyper_dev, int decay, int norm_p,
+                         int T, const float* abc, const int* restart_after, int n_restart, float eps,
+                         int compute_dtype, int32_t* sel_out,
+                         const int32_t* carry_rows, float* carry_mu_dev, int defer,
+                         void* workspace, size_t workspace_bytes,
+                         int* status_dev, void* stream);
+
+/*
  * dion3_decay_rows -- applies a decay that dion3_step_carry left pending:
  *   M[b][rows[b][j]][:] <- mu * M[b][rows[b][j]][:]  (fp32, one rounding)
  * for j < k and rows in [0, n); other entries are skipped.  List each row once (as sel_out

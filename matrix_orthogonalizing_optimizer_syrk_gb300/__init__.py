@@ -65,6 +65,9 @@ SIGNATURES = {
                                   _c_int, _c_p, _c_p, _c_f, _c_int, _c_p, _c_sz, _c_p, _c_p, ctypes.POINTER(_c_p),
                                   _c_int]),
     "dion3_decay_rows": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_p, _c_int, _c_f, _c_p]),
+    "dion3_step_dev_carry": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_p,
+                                      _c_int, _c_int, _c_int, ctypes.POINTER(_c_f), ctypes.POINTER(_c_int), _c_int,
+                                      _c_f, _c_int, _c_p, _c_p, _c_p, _c_int, _c_p, _c_sz, _c_p, _c_p]),
     "dion3_gram_ns_noalloc": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_i64, _c_i64, _c_int, _c_p, _c_i64, _c_i64,
                                        _c_int, _c_int, ctypes.POINTER(_c_f), ctypes.POINTER(_c_int), _c_int, _c_f,
                                        _c_int, _c_p, _c_p]),
@@ -285,11 +288,22 @@ def step(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, f=(1, 4), mu: float 
     ``defer``: leave this step's decay of M[S,:] by ``mu`` pending (M[S,:] keeps M + G) and
     pass ``carry=(sel, mu)`` -- the returned rows and this mu -- to the next call, whose momentum
     pass applies it (dion3_step_carry in include/dion3.h); ``decay_rows`` applies it on its own.
-    The state that results is bit-identical to that of plain steps.
+    The state that results is bit-identical to that of plain steps.  With ``hyper`` the carried
+    mu is a one-element fp32 device tensor, read as the pending factor and, with ``defer``,
+    overwritten with this step's mu (dion3_step_dev_carry): ``carry=(sel, mu_word)`` every call,
+    mu_word set to 1.0 before the first (``carry=(None, mu_word)`` carries nothing in).
     """
     carrying = carry is not None or defer
+    mu_word = None
     if carrying and hyper is not None:
-        raise ValueError("carry/defer take host hyperparameters (hyper must be None)")
+        if carry is None or not isinstance(carry[1], torch.Tensor):
+            raise ValueError("with hyper, carry=(rows or None, mu_word) with mu_word a device fp32 tensor")
+        mu_word = carry[1]
+        _cuda(mu_word, "carried mu")
+        if mu_word.dtype != torch.float32 or mu_word.numel() < 1:
+            raise ValueError("the carried mu word must be an fp32 device tensor")
+    elif carry is not None and isinstance(carry[1], torch.Tensor):
+        raise ValueError("a device carried mu needs hyper (device hyperparameters)")
     for t, name in ((W, "W"), (M, "M"), (G, "G")):
         _cuda(t, name)
         if not t.is_contiguous():
@@ -316,6 +330,7 @@ def step(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, f=(1, 4), mu: float 
     carry_rows, carry_mu = None, 1.0
     if carry is not None:
         carry_rows, carry_mu = carry
+    if carry_rows is not None:
         _cuda(carry_rows, "carry rows")
         if carry_rows.dtype != torch.int32 or tuple(carry_rows.shape) != shape or not carry_rows.is_contiguous():
             raise ValueError(f"carry rows must be contiguous int32 of shape {shape}")
@@ -329,6 +344,14 @@ def step(W: torch.Tensor, M: torch.Tensor, G: torch.Tensor, f=(1, 4), mu: float 
             raise ValueError("hyper must be a contiguous fp32 device tensor {mu, eta, wd}")
         if events is not None:
             raise ValueError("events and hyper cannot be combined")
+        if carrying:
+            rc = lib().dion3_step_dev_carry(batch, n, m, _ptr(W), _ptr(M), _ptr(G), _dt(G), f_num, f_den,
+                                            _ptr(hyper), int(bool(decay)), norm_p, T, flat, rarr, nr, float(eps),
+                                            _dtype_code(compute), _ptr(sel_out), _ptr(carry_rows), _ptr(mu_word),
+                                            int(bool(defer)), _ptr(workspace), workspace.numel(), _ptr(status),
+                                            _stream_ptr(M.device))
+            _check(rc, "dion3_step_dev_carry")
+            return sel_out
         rc = lib().dion3_step_dev(batch, n, m, _ptr(W), _ptr(M), _ptr(G), _dt(G), f_num, f_den, _ptr(hyper),
                                   int(bool(decay)), norm_p, T, flat, rarr, nr, float(eps), _dtype_code(compute),
                                   _ptr(sel_out), _ptr(workspace), workspace.numel(), _ptr(status),

@@ -568,11 +568,12 @@ int step_impl(int batch, int n, int m, float* W, float* M, const void* G, int g_
               const int* restart_after, int n_restart, float eps, int compute_dtype, int32_t* sel_out,
               void* workspace, size_t workspace_bytes, int* status_dev, void* stream, void* const* events,
               int n_events, bool cols = false, const int32_t* carry_rows = nullptr, float carry_mu = 1.f,
-              bool defer = false) {
+              bool defer = false, float* carry_mu_dev = nullptr) {
   if (n_events < 0 || (n_events > 0 && events == nullptr)) return DION3_EINVAL;
   if (cols && (carry_rows != nullptr || defer)) return DION3_EUNSUPPORTED;
+  if (carry_mu_dev != nullptr && (reinterpret_cast<uintptr_t>(carry_mu_dev) & 3u) != 0) return DION3_EALIGN;
   if (carry_rows != nullptr) {
-    if (!std::isfinite(carry_mu)) return DION3_EINVAL;
+    if (carry_mu_dev == nullptr && !std::isfinite(carry_mu)) return DION3_EINVAL;
     // A caller-chosen S is read from sel_out: a carried list there would be the new S.
     if (norm_p == DION3_SELECT_GIVEN && carry_rows == sel_out) return DION3_EINVAL;
     if ((reinterpret_cast<uintptr_t>(carry_rows) & 3u) != 0) return DION3_EALIGN;
@@ -640,6 +641,7 @@ int step_impl(int batch, int n, int m, float* W, float* M, const void* G, int g_
     sa.carry_flag = reinterpret_cast<uint8_t*>(ws + L.carry);
     sa.carry_mu = carry_mu;
     sa.defer = defer;
+    sa.carry_mu_dev = carry_mu_dev;
   }
 
   // Phase boundaries for the caller's timing events (0: start ... 4: end).
@@ -746,6 +748,18 @@ int dion3_step_carry(int batch, int n, int m, float* W, float* M, const void* G,
   return step_impl(batch, n, m, W, M, G, g_dtype, f_num, f_den, mu, eta, wd, nullptr, false, norm_p, T, abc,
                    restart_after, n_restart, eps, compute_dtype, sel_out, workspace, workspace_bytes, status_dev,
                    stream, events, n_events, false, carry_rows, carry_mu, defer != 0);
+}
+
+int dion3_step_dev_carry(int batch, int n, int m, float* W, float* M, const void* G, int g_dtype, int f_num,
+                         int f_den, const float* hyper_dev, int decay, int norm_p, int T, const float* abc,
+                         const int* restart_after, int n_restart, float eps, int compute_dtype, int32_t* sel_out,
+                         const int32_t* carry_rows, float* carry_mu_dev, int defer, void* workspace,
+                         size_t workspace_bytes, int* status_dev, void* stream) {
+  if (hyper_dev == nullptr) return DION3_EINVAL;
+  if ((carry_rows != nullptr || defer != 0) && carry_mu_dev == nullptr) return DION3_EINVAL;
+  return step_impl(batch, n, m, W, M, G, g_dtype, f_num, f_den, 0.f, 0.f, 0.f, hyper_dev, decay != 0, norm_p, T,
+                   abc, restart_after, n_restart, eps, compute_dtype, sel_out, workspace, workspace_bytes, status_dev,
+                   stream, nullptr, 0, false, carry_rows, 1.f, defer != 0, carry_mu_dev);
 }
 
 int dion3_decay_rows(int batch, int n, int m, float* M, const int32_t* rows, int k, float mu, void* stream) {

@@ -130,6 +130,9 @@ struct StepArgs {
   uint8_t* carry_flag = nullptr;
   float carry_mu = 1.f;
   bool defer = false;
+  // Device form (graph capture): the pending factor is read from carry_mu_dev, and with defer
+  // pass C stores this step's mu there once it has been read.
+  float* carry_mu_dev = nullptr;
 };
 int step_momentum_keys(const StepArgs& a, cudaStream_t s);
 int step_select(const StepArgs& a, cudaStream_t s);

@@ -77,6 +77,7 @@ struct AArgs {
   int* status;
   const uint8_t* carry;  // [rows]: nonzero where an earlier step's decay of the row is pending
   float carry_mu;
+  const float* carry_mu_dev;  // when set (and carry is), the pending factor is read from here
 };
 
 // ------------------------------------------------------------------------------ pass A
@@ -90,6 +91,7 @@ __global__ void __launch_bounds__(256) momentum_keys_kernel(const AArgs a) {
       a.hyper ? __double2float_rn(__dsub_rn(1.0, __dmul_rn(__dmul_rn(static_cast<double>(a.hyper[1]), a.eta_scale),
                                                             static_cast<double>(a.hyper[2]))))
               : a.w_decay;
+  const float cm = (a.carry != nullptr && a.carry_mu_dev != nullptr) ? *a.carry_mu_dev : a.carry_mu;
   for (long long row = w0; row < a.rows; row += nw) {
     float* Mr = a.M + row * m;
     const TG* Gr = static_cast<const TG*>(a.G) + row * m;
@@ -100,7 +102,6 @@ __global__ void __launch_bounds__(256) momentum_keys_kernel(const AArgs a) {
     // A pending decay is applied first, rounded to fp32 on its own, so the row ends exactly as
     // if the earlier step had stored mu M and this pass then added G.
     const bool cr = a.carry != nullptr && a.carry[row] != 0;
-    const float cm = a.carry_mu;
     if constexpr (VEC) {
       for (int j = lane * 8; j < m; j += 256) {
         float g[8];
@@ -477,6 +478,7 @@ struct CArgs {
   float mu;
   const float* mu_dev;  // when set, mu is read from here
   const float* scale;
+  float* mu_out;  // when set, the mu of this step is stored here (a decay left pending)
 };
 
 template <typename T>
@@ -495,6 +497,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const CArgs a) {
   const long long w0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
   const float mu = a.mu_dev ? *a.mu_dev : a.mu;
+  if (a.mu_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *a.mu_out = mu;
   for (long long row = w0; row < a.rows; row += nw) {
     const long long b = row / a.k;
     const int i = a.sel[row];
@@ -636,6 +639,7 @@ int step_momentum_keys(const StepArgs& s, cudaStream_t st) {
   a.status = s.status;
   a.carry = s.carry_rows != nullptr ? s.carry_flag : nullptr;
   a.carry_mu = s.carry_mu;
+  a.carry_mu_dev = s.carry_mu_dev;
   if (a.rows == 0) return DION3_OK;
   if (a.carry != nullptr) {
     carry_flags_kernel<<<s.batch, 256, 0, st>>>(s.n, s.k, s.carry_rows, s.carry_flag);
@@ -704,6 +708,7 @@ int step_gather(const StepArgs& s, cudaStream_t st) {
   c.mu = s.mu;
   c.mu_dev = s.hyper;
   c.scale = s.scale;
+  c.mu_out = s.defer ? s.carry_mu_dev : nullptr;
   const bool vec = (s.m % 4 == 0) && aligned16(s.M) && (s.ldx % 8 == 0);
   switch (s.cdt) {
     case FP32:

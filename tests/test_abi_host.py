@@ -260,3 +260,21 @@ def test_decay_rows_validation(L):
 def test_carry_adds_one_launch():
     base = d3.step_launch_count(5, (2, 4), 1024)
     assert d3.step_launch_count(5, (2, 4), 1024, carry=True) == base + 1
+
+
+def test_step_dev_carry_validation(L):
+    r = (ctypes.c_int * 1)(2)
+    SEL = ctypes.c_void_p(0x20000)
+    MU = ctypes.c_void_p(0x30000)
+
+    def call(hyper=FAKE, carry=SEL, mu=MU, defer=1, p=1, ws=FAKE, wsb=1 << 40):
+        return L.dion3_step_dev_carry(1, 64, 128, FAKE, FAKE, FAKE, 0, 1, 4, hyper, 0, p, 5, _abc(5), r, 1, 1e-7, 0,
+                                      SEL, carry, mu, defer, ws, wsb, NULL, NULL)
+
+    assert call(hyper=NULL) == 1
+    assert call(mu=NULL) == 1                              # a carried list needs the mu word
+    assert call(carry=NULL, mu=NULL) == 1                  # so does defer
+    assert call(carry=NULL, mu=NULL, defer=0, ws=NULL) == 3  # neither: the plain device step
+    assert call(mu=ctypes.c_void_p(0x30002)) == 5
+    assert call(p=0) == 1                                  # given S in sel_out cannot be the carried list
+    assert call(ws=NULL) == 3

@@ -101,3 +101,52 @@ def test_decay_off_ignores_wd():
     d3.step(Wb, Mb, G, f=(1, 4), mu=0.95, eta=0.01, wd=0.0, abc=ABC, restart_after=(2,))
     torch.cuda.synchronize()
     assert torch.equal(Wa, Wb) and torch.equal(Ma, Mb)
+
+
+@pytest.mark.parametrize("n,m,f,compute", [(128, 512, (1, 4), torch.float16), (96, 1004, (1, 8), torch.float16)])
+def test_graph_replay_with_carried_decay(n, m, f, compute):
+    """dion3_step_dev_carry captured once: each replay applies the previous replay's decay (its mu
+    kept in a device word that starts at 1.0) and leaves its own pending.  After the last replay
+    and dion3_decay_rows, W, M and every selection equal eager plain steps bit for bit."""
+    batch = 3
+    W0 = synthetic.gaussian((batch, n, m), seed=13, std=0.02, device=DEV)
+    M0 = synthetic.gaussian((batch, n, m), seed=14, std=0.01, device=DEV)
+    Gs = [synthetic.lowrank_batch(batch, n, m, base_seed=750 + 10 ** 6 * t, dtype=torch.bfloat16, device=DEV)
+          for t in range(len(SCHEDULE))]
+    k = d3.k_of(n, *f)
+    ws_bytes = d3.workspace_bytes_step(batch, n, m, f[0], f[1], 1, compute, 2)
+
+    We, Me = W0.clone(), M0.clone()
+    sel_e = []
+    for t, (mu, eta, wd) in enumerate(SCHEDULE):
+        sel_e.append(d3.step(We, Me, Gs[t], f=f, mu=mu, eta=eta, wd=wd, abc=ABC, restart_after=(2, 4),
+                             compute=compute).clone())
+
+    Wg, Mg = W0.clone(), M0.clone()
+    G = torch.empty_like(Gs[0])
+    hyper = torch.tensor(SCHEDULE[0], dtype=torch.float32, device=DEV)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=DEV)
+    sel = torch.full((batch, k), -1, dtype=torch.int32, device=DEV)   # nothing pending yet
+    mu_word = torch.ones(1, dtype=torch.float32, device=DEV)          # a factor of 1 changes nothing
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    # warm the library's per-device caches on scratch state
+    d3.step(W0.clone(), M0.clone(), Gs[0], f=f, abc=ABC, restart_after=(2, 4), compute=compute, hyper=hyper,
+            decay=True, workspace=ws, sel_out=sel.clone(), status=status,
+            carry=(None, torch.ones(1, dtype=torch.float32, device=DEV)), defer=True)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        d3.step(Wg, Mg, G, f=f, abc=ABC, restart_after=(2, 4), compute=compute, hyper=hyper, decay=True,
+                workspace=ws, sel_out=sel, status=status, carry=(sel, mu_word), defer=True)
+    for t, vals in enumerate(SCHEDULE):
+        G.copy_(Gs[t])
+        hyper.copy_(torch.tensor(vals, dtype=torch.float32))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(sel, sel_e[t]), f"replay {t}: selection differs"
+        assert float(mu_word.item()) == float(np.float32(vals[0])), f"replay {t}: carried mu not stored"
+    assert int(status.item()) == 0
+    assert np.array_equal(bits32(Wg), bits32(We))
+    d3.decay_rows(Mg, sel, float(mu_word.item()))
+    torch.cuda.synchronize()
+    assert np.array_equal(bits32(Mg), bits32(Me))
