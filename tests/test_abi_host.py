@@ -278,3 +278,45 @@ def test_step_dev_carry_validation(L):
     assert call(mu=ctypes.c_void_p(0x30002)) == 5
     assert call(p=0) == 1                                  # given S in sel_out cannot be the carried list
     assert call(ws=NULL) == 3
+
+
+def _declared_signatures():
+    """name -> list of parameter type strings, from the header's prototypes."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b[\w\s\*]+?\b(dion3_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        params = " ".join(m.group(2).split())
+        if params in ("", "void"):
+            out[m.group(1)] = []
+        else:
+            out[m.group(1)] = [p.strip() for p in params.split(",")]
+    return out
+
+
+def _ctype_kind(t):
+    if t in (ctypes.c_float,):
+        return "float"
+    if t in (ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_longlong):
+        return "int"
+    return "ptr"
+
+
+def _decl_kind(p):
+    if "*" in p:
+        return "ptr"
+    if p.startswith("float"):
+        return "float"
+    return "int"
+
+
+def test_binding_signatures_match_header():
+    """Every prototype in the header has the binding's argument count and kinds (pointer, integer,
+    float), so a change on one side cannot silently shift the other's arguments."""
+    decl = _declared_signatures()
+    assert set(decl) == set(_declared_functions())
+    for name, params in decl.items():
+        _, args = d3.SIGNATURES[name]
+        assert len(args) == len(params), f"{name}: header has {len(params)} parameters, binding {len(args)}"
+        for i, (p, a) in enumerate(zip(params, args)):
+            assert _decl_kind(p) == _ctype_kind(a), f"{name} argument {i} ({p}): binding declares {a}"
