@@ -84,6 +84,41 @@ def gram_flops(k: int, m: int, T: int = T_ITERS, restarts=RESTARTS) -> int:
     return (4 * T - 3) * k ** 3 + 3 * m * k * k + r * 3 * (m * k * k - k ** 3)
 
 
+def gram_chain_products(k: int, m: int, T: int = T_ITERS, restarts=RESTARTS, es: int = 2):
+    """(useful FLOPs, algorithmic DRAM bytes) of each product of one matrix's Gram-NS chain in a
+    Dion3 step, in launch order (k > 128: separate products; 16-bit iterates of es bytes; the
+    last product is the fused W update, which reads and writes k fp32 rows of W)."""
+    xxt = (k * k * m, (k * m + k * k) * es)            # X X^T: reads X, writes R
+    poly = (k ** 3, 2 * k * k * es)                     # a I + b R + c R^2: reads R, writes Z
+    prod = (k ** 3, 3 * k * k * es)                     # Q Z, R Z, (R Z) Z: two in, one out
+    qx = (2 * k * k * m, (k * k + 2 * k * m) * es)      # restart: reads Q, X; writes X
+    wupd = (2 * k * k * m, (k * k + k * m) * es + 8 * k * m)
+    seq, q_identity = [xxt], True
+    for t in range(1, T + 1):
+        seq.append(poly)
+        if q_identity:
+            q_identity = False
+        else:
+            seq.append(prod)
+        if t in restarts:
+            seq += [qx, xxt]
+            q_identity = True
+        elif t < T:
+            seq += [prod, prod]
+    seq.append(wupd)
+    return seq
+
+
+def gram_chain_bound_ms(mbs, tc_peak_tflops: float, hbm_gbs: float) -> float:
+    """Attainable time of the product chains of megabatches [(B, n, m)]: each product takes at
+    least its useful FLOPs at the tensor peak and its algorithmic bytes at the copy bandwidth."""
+    total = 0.0
+    for B, n, m in mbs:
+        for f, b in gram_chain_products(k_rows(n), m):
+            total += max(B * f / (tc_peak_tflops * 1e12), B * b / (hbm_gbs * 1e9))
+    return total * 1e3
+
+
 def k_rows(n: int) -> int:
     return -((-n * F[0]) // F[1])
 
@@ -273,6 +308,8 @@ def run_ours(args):
     bytesC = sum(GATHER_BYTES * x["B"] * k_rows(x["n"]) * x["m"] for x in mbs)
     flops = sum(float(x["B"] * gram_flops(k_rows(x["n"]), x["m"])) for x in mbs)
     ph = {n: sum(pm[i] for pm in per_mb) for i, n in enumerate(names)}
+    # the chain's attainable time: per product, the slower of its tensor and HBM times
+    bound_ms = gram_chain_bound_ms([(x["B"], x["n"], x["m"]) for x in mbs], tc_sus, hbm)
     phases = {
         "momentum_keys": {"ms": ph["momentum_keys"], "GB/s": bytesA / ph["momentum_keys"] / 1e6,
                           "frac_hbm": bytesA / ph["momentum_keys"] / 1e6 / hbm,
@@ -282,7 +319,9 @@ def run_ours(args):
                    "algorithmic_bytes": bytesC},
         "gram_ns_products": {"ms": ph["gram_ns_products"], "TFLOP/s": flops / ph["gram_ns_products"] / 1e9,
                              "frac_tensor_sustained": flops / ph["gram_ns_products"] / 1e9 / tc_sus,
-                             "useful_flops": flops},
+                             "useful_flops": flops,
+                             "attainable_ms": bound_ms,
+                             "frac_of_attainable": bound_ms / ph["gram_ns_products"]},
         "per_megabatch_ms": [{"shape": f"{x['B']}x{x['n']}x{x['m']}", "ms": sum(pm)} for x, pm in zip(mbs, per_mb)],
     }
     dominant = max(names, key=lambda n: ph[n])

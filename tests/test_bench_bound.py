@@ -1,0 +1,44 @@
+"""Host checks of bench.py's attainable-time model of the Gram-NS product chain: its product list
+follows the library's launch sequence, and its useful FLOPs add up to the pages' closed form."""
+
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+import matrix_orthogonalizing_optimizer_syrk_gb300 as d3  # noqa: E402
+
+SCHEDULES = [(5, (2, 4)), (5, ()), (5, (2,)), (3, (1, 2)), (1, ()), (8, (3, 6))]
+
+
+@pytest.mark.parametrize("T,restarts", SCHEDULES)
+def test_product_list_follows_the_launch_sequence(T, restarts):
+    assert len(bench.gram_chain_products(1024, 4096, T, restarts)) == d3.gram_core_launch_count(T, restarts, 1024)
+
+
+@pytest.mark.parametrize("T,restarts", SCHEDULES)
+@pytest.mark.parametrize("k,m", [(1024, 4096), (1024, 11008), (256, 300)])
+def test_useful_flops_equal_the_closed_form(T, restarts, k, m):
+    """(4T + 3 alpha - 3) k^3 + r 3 (alpha - 1) k^3, the pages' FLOP count of Gram-NS with r restarts."""
+    flops = sum(f for f, _ in bench.gram_chain_products(k, m, T, restarts))
+    assert flops == bench.gram_flops(k, m, T, restarts)
+
+
+def test_single_iteration_bytes():
+    """T = 1: X X^T, the polynomial, the fused W update; 16-bit iterates, fp32 W."""
+    k, m = 256, 1000
+    seq = bench.gram_chain_products(k, m, 1, ())
+    assert [b for _, b in seq] == [2 * (k * m + k * k), 2 * 2 * k * k, 2 * (k * k + k * m) + 8 * k * m]
+
+
+def test_bound_is_the_slower_of_tensor_and_hbm_per_product():
+    k, m = 1024, 4096
+    fast_hbm = bench.gram_chain_bound_ms([(1, 4096, m)], 1000.0, 1e12)
+    flops = sum(f for f, _ in bench.gram_chain_products(k, m))
+    assert fast_hbm == pytest.approx(flops / 1e15 * 1e3)
+    fast_tc = bench.gram_chain_bound_ms([(1, 4096, m)], 1e12, 1000.0)
+    nbytes = sum(b for _, b in bench.gram_chain_products(k, m))
+    assert fast_tc == pytest.approx(nbytes / 1e12 * 1e3)
