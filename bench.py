@@ -460,7 +460,7 @@ def run_e2e(torch, d3, mbs, ws, status, args, dev, dist):
     return {"value": ms_job, "unit": "ms per megabatch step (both 7B shape groups)",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "path": "G copied from pinned host memory on a copy stream (step t+1's copy overlaps step t), "
-                    "dion3_step through the C ABI, selected rows copied back every step"}
+                    "dion3_step_carry (decay carried) through the C ABI, selected rows copied back every step"}
 
 
 def _time_calls(torch, fn, reps, flush=None):
