@@ -47,7 +47,7 @@ extern "C" {
 typedef enum {
   DION3_OK = 0,
   DION3_EINVAL = 1,        /* a null pointer, negative or inconsistent size, bad schedule */
-  DION3_EUNSUPPORTED = 2,  /* valid but outside what this build supports (dtype mix, limits) */
+  DION3_EUNSUPPORTED = 2,  /* valid but outside what the library supports (dtype mix, limits) */
   DION3_EWORKSPACE = 3,    /* workspace missing or smaller than the query says */
   DION3_ECUDA = 4,         /* a CUDA call (launch, tensor-map encode, attribute) failed */
   DION3_EALIGN = 5         /* a pointer, leading dimension or stride breaks the 16-byte rule */
