@@ -42,3 +42,21 @@ def test_bound_is_the_slower_of_tensor_and_hbm_per_product():
     fast_tc = bench.gram_chain_bound_ms([(1, 4096, m)], 1e12, 1000.0)
     nbytes = sum(b for _, b in bench.gram_chain_products(k, m))
     assert fast_tc == pytest.approx(nbytes / 1e12 * 1e3)
+
+
+def test_carried_step_passes_the_previous_selection():
+    """The timed loop's step: the first call carries nothing in, every later call carries the
+    previous call's rows (the same buffer it writes) with mu, and every call defers its own decay."""
+    calls = []
+
+    class FakeLib:
+        @staticmethod
+        def step(W, M, G, **kw):
+            calls.append(kw)
+
+    x = {"W": "W", "M": "M", "Gs": ["G0", "G1"], "sel": "sel"}
+    for s in range(3):
+        bench.carried_step(FakeLib, x, s % 2, "ws", "status")
+    assert calls[0]["carry"] is None
+    assert all(c["carry"] == ("sel", bench.MU) for c in calls[1:])
+    assert all(c["defer"] is True and c["sel_out"] == "sel" for c in calls)
