@@ -157,3 +157,43 @@ def test_restart_schedule_validation(jordan):
             oracle.gram_ns(X, [jordan] * 5, bad)
     with pytest.raises(ValueError):
         oracle.gram_ns(_rand(5, 3, 0), [jordan] * 5)
+
+
+def test_odd_poly_matches_library_polynomial_evaluation(jordan):
+    """Muon blog, 'Doing an SVD without an SVD': each step applies the odd quintic
+    p(x) = a x + b x^3 + c x^5 to the singular values.  numpy's polynomial evaluator, given the
+    coefficient vector (0, a, 0, b, 0, c), is the independent definition."""
+    x = np.linspace(-1.5, 1.5, 601)
+    for a, b, c in [jordan, (1.5, -0.5, 0.0), (2.0, -1.5, 0.5)]:
+        ref = np.polynomial.polynomial.polyval(x, [0.0, a, 0.0, b, 0.0, c])
+        np.testing.assert_allclose(oracle.odd_poly(x, a, b, c), ref, rtol=1e-13, atol=1e-14)
+        # odd: p(-x) = -p(x), and p(0) = 0
+        xp = np.linspace(0.0, 1.5, 301)
+        np.testing.assert_allclose(oracle.odd_poly(-xp, a, b, c), -oracle.odd_poly(xp, a, b, c), rtol=1e-14, atol=0)
+        assert oracle.odd_poly(0.0, a, b, c) == 0.0
+
+
+def test_composite_scalar_is_the_iterated_polynomial_and_the_svd_map(jordan):
+    """(p_T o ... o p_1) in the order given: against the library evaluator applied T times, and
+    against the singular values that numpy's SVD finds in the oracle's standard NS output."""
+    abc = [(1.9, -1.1, 0.2), jordan, (1.5, -0.5, 0.0)]
+    x = np.linspace(0.0, 1.0, 1001)
+    ref = x.copy()
+    for a, b, c in abc:
+        ref = np.polynomial.polynomial.polyval(ref, [0.0, a, 0.0, b, 0.0, c])
+    np.testing.assert_allclose(oracle.composite_scalar(x, abc), ref, rtol=1e-12, atol=1e-14)
+    # the order matters: reversing the table gives a different map
+    assert np.max(np.abs(oracle.composite_scalar(x, abc[::-1]) - ref)) > 1e-3
+    # a matrix with known singular values: SVD of the standard-NS output
+    sig = np.array([0.9, 0.5, 0.3, 0.1, 0.02])
+    X, _, _ = _with_singular_values(5, 12, sig, seed=31)
+    got = np.sort(np.linalg.svd(oracle.ns_standard(X, abc, eps=0.0), compute_uv=False))
+    expect = np.sort(oracle.composite_scalar(sig / np.linalg.norm(sig), abc))
+    np.testing.assert_allclose(got, expect, rtol=1e-11)
+
+
+def test_composite_scalar_cubic_converges_to_sign():
+    """Dion3 summary, prerequisite 'polar decomposition': iterating the cubic
+    (1.5, -0.5, 0) drives every x in (0, sqrt(3)) to 1 (and -x to -1): the scalar polar factor."""
+    x = np.concatenate([np.linspace(0.05, 1.7, 200), -np.linspace(0.05, 1.7, 200)])
+    np.testing.assert_allclose(oracle.composite_scalar(x, [(1.5, -0.5, 0.0)] * 80), np.sign(x), rtol=0, atol=1e-12)
