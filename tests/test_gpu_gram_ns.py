@@ -103,20 +103,33 @@ def test_output_singular_values_in_band():
 
 @pytest.mark.parametrize("shape,count", [((4096, 4096), 128), ((4096, 11008), 96)])
 def test_megabatch_full_size_sampled(shape, count):
-    """7B-shaped megabatches (bf16 momenta, fp16 iterates, restarts after 2 and 4); the oracle checks
-    matrices 0, B/2 and B-1."""
+    """7B-shaped megabatches at full size (bf16 momenta): float16 iterates (the paper's precision)
+    and bfloat16 iterates, each with the benchmark's restarts after 2 and 4 and with the paper's
+    single restart after 2; the oracle checks matrices 0, B/2 and B-1 at 3e-2.
+
+    One oracle result per matrix serves every schedule: by Theorem 2 the restart positions change
+    nothing in exact arithmetic (the oracle's Gram NS equals standard NS to 1e-10 for every
+    schedule), they only bound the growth of rounding errors in 16-bit iterates."""
     n, m = shape
     base = 3000 + (0 if m == n else 1000)
     X = torch.empty((count, n, m), dtype=torch.bfloat16, device=DEV)
     for i in range(count):
         synthetic.lowrank_plus_noise(n, m, base + i, dtype=torch.bfloat16, device=DEV, out=X[i])
-    status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    O = d3.gram_ns(X, ABC, (2, 4), status=status)
-    torch.cuda.synchronize()
-    assert int(status.item()) == 0
-    for i in (0, count // 2, count - 1):
-        ref = oracle.gram_ns(to64(X[i]), ABC, (2, 4))
-        assert rel_frob(to64(O[i]), ref) <= 3e-2
+    idx = (0, count // 2, count - 1)
+    refs = {i: oracle.gram_ns(to64(X[i]), ABC, (2, 4)) for i in idx}
+    O = torch.empty_like(X)
+    worst = {}
+    for compute in (torch.float16, torch.bfloat16):
+        for restarts in ((2, 4), (2,)):
+            status = torch.zeros(1, dtype=torch.int32, device=DEV)
+            d3.gram_ns(X, ABC, restarts, compute=compute, out=O, status=status)
+            torch.cuda.synchronize()
+            assert int(status.item()) == 0
+            errs = [rel_frob(to64(O[i]), refs[i]) for i in idx]
+            worst[(str(compute), restarts)] = max(errs)
+    print(f"{count}x{n}x{m} worst rel. Frobenius error per (iterates, restarts):", worst)
+    for key, err in worst.items():
+        assert err <= 3e-2, f"{key}: {err:.4g}"
 
 
 @pytest.mark.parametrize("n,m", [(128, 512), (65, 300), (64, 64), (127, 130)])
