@@ -60,7 +60,10 @@ typedef enum { DION3_BF16 = 0, DION3_FP16 = 1, DION3_FP32 = 2 } dion3_dtype;
 #define DION3_SELECT_GIVEN 0
 
 /* Bits OR-ed into *status_dev by kernels. */
-#define DION3_DEV_NONFINITE 0x1 /* a non-finite momentum key, norm or input value was seen */
+#define DION3_DEV_NONFINITE 0x1 /* a non-finite momentum key, norm or input value was seen, or
+                                   the last product of the orthogonalisation wrote a non-finite
+                                   value (into Out, or into W by the row update): the iteration
+                                   diverged ("half precision and numerical stability") */
 #define DION3_DEV_TIMEOUT   0x2 /* a bounded wait gave up; outputs of that call are undefined */
 #define DION3_DEV_SELECT    0x4 /* row selection could not certify k rows (internal error), or a
                                    caller-chosen S was not k distinct ascending rows in [0, n) */
@@ -136,7 +139,7 @@ size_t dion3_gram_ns_workspace_bytes(int batch, int n, int m, int x_dtype, int c
  *         256-byte aligned.
  *   Errors: EINVAL (n > m, T < 1, schedule), EWORKSPACE, EALIGN (Out, workspace),
  *           EUNSUPPORTED (fp32 compute with a 16-bit output), ECUDA.
- *   Device: DION3_DEV_NONFINITE if a norm is not finite.
+ *   Device: DION3_DEV_NONFINITE if a norm or an element of Out is not finite.
  */
 int dion3_gram_ns(int batch, int n, int m,
                   const void* X, int64_t ldx, int64_t strideX, int x_dtype,
@@ -169,7 +172,7 @@ size_t dion3_ns_standard_workspace_bytes(int batch, int n, int m, int compute_dt
  *   always copied, prescaled, into the workspace).
  *   Errors: EINVAL (n > m, T < 1), EWORKSPACE, EALIGN (Out, workspace), EUNSUPPORTED (fp32
  *           compute with a 16-bit output), ECUDA.
- *   Device: DION3_DEV_NONFINITE if a norm is not finite.
+ *   Device: DION3_DEV_NONFINITE if a norm or an element of Out is not finite.
  */
 int dion3_ns_standard(int batch, int n, int m,
                       const void* X, int64_t ldx, int64_t strideX, int x_dtype,
@@ -217,7 +220,8 @@ size_t dion3_step_workspace_bytes(int batch, int n, int m, int f_num, int f_den,
  *   sel_out : int32 [batch][k] device output, ascending row indices.
  *   Limits: n <= 16384 and m <= 65536 (exact selection); 0 < f_num <= f_den.
  *   W, M, G, sel_out 16-byte aligned.  Errors as dion3_gram_ns.
- *   Device: DION3_DEV_NONFINITE (a non-finite momentum or norm), DION3_DEV_SELECT.
+ *   Device: DION3_DEV_NONFINITE (a non-finite momentum or norm, or a non-finite updated W
+ *           row element), DION3_DEV_SELECT.
  */
 int dion3_step(int batch, int n, int m,
                float* W, float* M, const void* G, int g_dtype,
@@ -370,10 +374,15 @@ int dion3_decay_rows(int batch, int n, int m, float* M, const int32_t* rows, int
  * (no counterpart in the paper).  Same arguments and results as dion3_gram_ns, minus the
  * workspace: the scratch comes from an array of DION3_NOALLOC_SCRATCH_BYTES compiled into the
  * library, resident on every GPU that loads the library until the process exits.
+ *   - Arguments are checked exactly as dion3_gram_ns checks them, in the same order, so a bad
+ *     call returns the same code from either entry point.
  *   - Sizes whose workspace (dion3_gram_ns_workspace_bytes, plus the copy of a misaligned X)
- *     exceeds DION3_NOALLOC_SCRATCH_BYTES are rejected with DION3_EWORKSPACE, nothing enqueued.
+ *     exceeds DION3_NOALLOC_SCRATCH_BYTES are then rejected with DION3_EWORKSPACE, nothing
+ *     enqueued.
  *   - The first call on a device looks up the array's device address (with that device
- *     current) and keeps it; make that first call before any stream capture.
+ *     current) and keeps it; make that first call before any stream capture.  The address
+ *     belongs to the device's primary context: after cudaDeviceReset on that device it is
+ *     stale, so do not call this entry point there again in the same process.
  *   - It allocates nothing and frees nothing.
  *   - Every call uses the same array and leaves its contents behind; nothing in it needs to
  *     start at zero.  Calls whose work overlaps on the GPU (other streams, other host

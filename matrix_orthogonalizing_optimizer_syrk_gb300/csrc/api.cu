@@ -183,7 +183,8 @@ int run_core(const Core& c, cudaStream_t s) {
     g.status = c.status;
     return gemm(g, s);
   };
-  auto gen = [&](const Mat& Q, const Mat& X, float alpha, const float* ab, int epi, const Mat& D) {
+  // `last`: the product that writes the result (Out, or W through the row update).
+  auto gen = [&](const Mat& Q, const Mat& X, float alpha, const float* ab, int epi, const Mat& D, bool last) {
     GemmCall g;
     g.batch = c.batch;
     g.M = c.n;
@@ -206,6 +207,7 @@ int run_core(const Core& c, cudaStream_t s) {
       g.eta_scale = c.eta_scale;
     }
     g.status = c.status;
+    g.check_finite = last;
     return gemm(g, s);
   };
 
@@ -237,7 +239,7 @@ int run_core(const Core& c, cudaStream_t s) {
         Xn.stride = static_cast<int64_t>(c.n) * c.L.ldm;
         Xn.dtype = c.cdt;
         next_x ^= 1;
-        rc = gen(nn(Qb), Xcur, 1.f, xs, EPI_GEN, Xn);
+        rc = gen(nn(Qb), Xcur, 1.f, xs, EPI_GEN, Xn, false);
         if (rc) return rc;
         Xcur = Xn;
         xs = nullptr;
@@ -246,8 +248,8 @@ int run_core(const Core& c, cudaStream_t s) {
       }
       t0 = t1 + 1;
     }
-    if (c.wupd) return gen(nn(Qb), Xcur, c.w_alpha, xs, EPI_WUPD, none);
-    return gen(nn(Qb), Xcur, 1.f, xs, EPI_GEN, c.Out);
+    if (c.wupd) return gen(nn(Qb), Xcur, c.w_alpha, xs, EPI_WUPD, none, true);
+    return gen(nn(Qb), Xcur, 1.f, xs, EPI_GEN, c.Out, true);
   }
 
   bool q_identity = true;
@@ -281,7 +283,7 @@ int run_core(const Core& c, cudaStream_t s) {
       Xn.stride = static_cast<int64_t>(c.n) * c.L.ldm;
       Xn.dtype = c.cdt;
       next_x ^= 1;
-      rc = gen(nn(Qb), Xcur, 1.f, xs, EPI_GEN, Xn);
+      rc = gen(nn(Qb), Xcur, 1.f, xs, EPI_GEN, Xn, false);
       if (rc) return rc;
       Xcur = Xn;
       xs = nullptr;
@@ -295,8 +297,8 @@ int run_core(const Core& c, cudaStream_t s) {
       if (rc) return rc;
     }
   }
-  if (c.wupd) return gen(nn(Qb), Xcur, c.w_alpha, xs, EPI_WUPD, none);
-  return gen(nn(Qb), Xcur, 1.f, xs, EPI_GEN, c.Out);
+  if (c.wupd) return gen(nn(Qb), Xcur, c.w_alpha, xs, EPI_WUPD, none, true);
+  return gen(nn(Qb), Xcur, 1.f, xs, EPI_GEN, c.Out, true);
 }
 
 }  // namespace
@@ -395,10 +397,14 @@ size_t dion3_gram_ns_workspace_bytes(int batch, int n, int m, int x_dtype, int c
   return gram_layout(batch, n, m, query_needs_copy(m, x_dtype, compute_dtype), compute_dtype, n_restart).total;
 }
 
-int dion3_gram_ns(int batch, int n, int m, const void* X, int64_t ldx, int64_t strideX, int x_dtype, void* Out,
-                  int64_t ldo, int64_t strideO, int out_dtype, int T, const float* abc, const int* restart_after,
-                  int n_restart, float eps, int compute_dtype, void* workspace, size_t workspace_bytes,
-                  int* status_dev, void* stream) {
+}  // extern "C"
+
+namespace dion3 {
+
+int gram_ns_validate(int batch, int n, int m, const void* X, int64_t ldx, int64_t strideX, int x_dtype,
+                     const void* Out, int64_t ldo, int64_t strideO, int out_dtype, int T, const float* abc,
+                     const int* restart_after, int n_restart, float eps, int compute_dtype, size_t* need) {
+  *need = 0;
   if (batch < 0 || n < 0 || m < 0) return DION3_EINVAL;
   if (!dtype_valid(x_dtype) || !dtype_valid(out_dtype) || !dtype_valid(compute_dtype)) return DION3_EINVAL;
   if (int rc = check_schedule(T, abc, restart_after, n_restart)) return rc;
@@ -410,6 +416,25 @@ int dion3_gram_ns(int batch, int n, int m, const void* X, int64_t ldx, int64_t s
   if (ldx < m || ldo < m) return DION3_EINVAL;
   if (batch > 1 && (strideX < n * ldx || strideO < n * ldo)) return DION3_EINVAL;
   if (!al16(Out) || !ld_ok(ldo, out_dtype) || (batch > 1 && !ld_ok(strideO, out_dtype))) return DION3_EALIGN;
+  const bool x_aligned = al16(X) && ld_ok(ldx, x_dtype) && (batch <= 1 || ld_ok(strideX, x_dtype));
+  const bool need_copy = x_dtype != compute_dtype || !x_aligned;
+  *need = gram_layout(batch, n, m, need_copy, compute_dtype, n_restart).total;
+  return DION3_OK;
+}
+
+}  // namespace dion3
+
+extern "C" {
+
+int dion3_gram_ns(int batch, int n, int m, const void* X, int64_t ldx, int64_t strideX, int x_dtype, void* Out,
+                  int64_t ldo, int64_t strideO, int out_dtype, int T, const float* abc, const int* restart_after,
+                  int n_restart, float eps, int compute_dtype, void* workspace, size_t workspace_bytes,
+                  int* status_dev, void* stream) {
+  size_t need = 0;
+  if (int rc = gram_ns_validate(batch, n, m, X, ldx, strideX, x_dtype, Out, ldo, strideO, out_dtype, T, abc,
+                                restart_after, n_restart, eps, compute_dtype, &need))
+    return rc;
+  if (need == 0) return DION3_OK;  // empty batch or n == 0: nothing to do
   const bool x_aligned = al16(X) && ld_ok(ldx, x_dtype) && (batch <= 1 || ld_ok(strideX, x_dtype));
   const bool need_copy = x_dtype != compute_dtype || !x_aligned;
   const GramLayout L = gram_layout(batch, n, m, need_copy, compute_dtype, n_restart);
@@ -526,6 +551,7 @@ int dion3_ns_standard(int batch, int n, int m, const void* X, int64_t ldx, int64
     u.beta = a;
     u.D = (t == T && direct) ? Om : Xb[cur ^ 1];
     u.status = status_dev;
+    u.check_finite = t == T;
     if ((rc = gemm(u, s))) return rc;
     cur ^= 1;
   }

@@ -8,28 +8,14 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "dev_common.cuh"
 #include "internal.h"
 
 namespace dion3 {
 namespace {
 
-template <typename T>
-__device__ __forceinline__ float to_f(T v);
-template <>
-__device__ __forceinline__ float to_f<float>(float v) { return v; }
-template <>
-__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
-template <>
-__device__ __forceinline__ float to_f<__half>(__half v) { return __half2float(v); }
-
-template <typename T>
-__device__ __forceinline__ T from_f(float v);
-template <>
-__device__ __forceinline__ float from_f<float>(float v) { return v; }
-template <>
-__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
-template <>
-__device__ __forceinline__ __half from_f<__half>(float v) { return __float2half_rn(v); }
+using dev::from_f;
+using dev::to_f;
 
 // Per-row sum of squares (fp32 FMA chain per lane, fixed warp tree): one warp per row,
 // grid-stride over all batch*n rows.

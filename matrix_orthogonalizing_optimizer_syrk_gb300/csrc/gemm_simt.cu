@@ -34,6 +34,8 @@ struct SParams {
   int w_rows;
   const float* eta_dev;
   double eta_scale;
+  int* status;
+  int check_finite;  // last product: flag non-finite stored values (DION3_DEV_NONFINITE)
 };
 
 template <int TS, bool B_MN, int EPI>
@@ -118,6 +120,7 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SParams p) {
   }
   const float alpha = p.eta_dev ? __double2float_rn(-__dmul_rn(static_cast<double>(*p.eta_dev), p.eta_scale)) : p.alpha;
   const float ab = alpha * (p.alpha_batch ? p.alpha_batch[b] : 1.f);
+  bool bad = false;
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const int r = mi * TS + ty * R + i;
@@ -139,13 +142,19 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SParams p) {
         if (p.beta != 0.f)
           v = fmaf(p.beta, p.C[static_cast<long long>(b) * p.sC + static_cast<long long>(r) * p.ldc + c], v);
         p.D[static_cast<long long>(b) * p.sD + static_cast<long long>(r) * p.ldd + c] = v;
+        bad |= !isfinite(v);
       } else {
         const int row = p.sel[static_cast<long long>(b) * p.ssel + r];
         if (row < 0 || row >= p.w_rows) continue;
-        p.W[static_cast<long long>(b) * p.sW + static_cast<long long>(row) * p.ldw + c] += v;
+        float* w = p.W + static_cast<long long>(b) * p.sW + static_cast<long long>(row) * p.ldw + c;
+        const float nw = *w + v;
+        *w = nw;
+        bad |= !isfinite(nw);
       }
     }
   }
+  if (p.check_finite && __syncthreads_or(bad) && threadIdx.x == 0 && p.status != nullptr)
+    atomicOr(p.status, DION3_DEV_NONFINITE);
 }
 
 template <int TS, bool B_MN, int EPI>
@@ -181,6 +190,8 @@ int launch(const GemmCall& g, cudaStream_t s) {
   p.w_rows = g.w_rows;
   p.eta_dev = g.eta_dev;
   p.eta_scale = g.eta_scale;
+  p.status = g.status;
+  p.check_finite = g.check_finite ? 1 : 0;
   if (g.batch > 65535) return DION3_EUNSUPPORTED;
   dim3 grid(p.tiles_per_batch, g.batch);
   simt_gemm_kernel<TS, B_MN, EPI><<<grid, NT, 0, s>>>(p);

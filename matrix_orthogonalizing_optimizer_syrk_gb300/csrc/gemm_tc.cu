@@ -23,7 +23,9 @@
 #include <cuda_fp16.h>
 
 #include <mutex>
+#include <type_traits>
 
+#include "dev_common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -86,6 +88,7 @@ struct KParams {
   long long spin_limit;
   const float* eta_dev;
   double eta_scale;
+  int check_finite;  // last product: flag non-finite stored values (DION3_DEV_NONFINITE)
 };
 
 // ----------------------------------------------------------------------------- tile order
@@ -133,23 +136,8 @@ __device__ __forceinline__ void decode_tile(const KParams& p, long long t, uint3
 }
 
 // ----------------------------------------------------------------------------- epilogue
-template <typename T>
-struct Out;
-template <>
-struct Out<float> {
-  static __device__ __forceinline__ float cvt(float v) { return v; }
-  static __device__ __forceinline__ float ld(const float* p) { return *p; }
-};
-template <>
-struct Out<__nv_bfloat16> {
-  static __device__ __forceinline__ __nv_bfloat16 cvt(float v) { return __float2bfloat16_rn(v); }
-  static __device__ __forceinline__ float ld(const __nv_bfloat16* p) { return __bfloat162float(*p); }
-};
-template <>
-struct Out<__half> {
-  static __device__ __forceinline__ __half cvt(float v) { return __float2half_rn(v); }
-  static __device__ __forceinline__ float ld(const __half* p) { return __half2float(*p); }
-};
+using dev::from_f;
+using dev::to_f;
 
 // 32 consecutive values of one row, written with 16-byte stores (caller checked alignment).
 template <typename T>
@@ -167,7 +155,7 @@ __device__ __forceinline__ void load_row32(const T* src, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < static_cast<int>(32 * sizeof(T) / 16); ++i) t[i] = s[i];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = Out<T>::ld(&tmp[i]);
+  for (int i = 0; i < 32; ++i) v[i] = to_f<T>(tmp[i]);
 }
 
 __device__ __forceinline__ bool aligned16(const void* p) {
@@ -191,7 +179,7 @@ __device__ __forceinline__ void epi_sym(const KParams& p, int b, int r, int c0, 
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int c = c0 + i;
-        if (c < p.N && c <= r) acc[i] = fmaf(p.beta, Out<T>::ld(crow + c), acc[i]);
+        if (c < p.N && c <= r) acc[i] = fmaf(p.beta, to_f<T>(crow[c]), acc[i]);
       }
     }
   }
@@ -202,7 +190,7 @@ __device__ __forceinline__ void epi_sym(const KParams& p, int b, int r, int c0, 
   }
   T o[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) o[i] = Out<T>::cvt(acc[i]);
+  for (int i = 0; i < 32; ++i) o[i] = from_f<T>(acc[i]);
   if (interior && aligned16(drow + c0)) {
     store_row32<T>(drow + c0, o);
 #pragma unroll
@@ -226,11 +214,11 @@ __device__ __forceinline__ void epi_gen(const KParams& p, int b, int r, int c0, 
     const T* crow = static_cast<const T*>(p.C) + static_cast<long long>(b) * p.sC + static_cast<long long>(r) * p.ldc;
 #pragma unroll
     for (int i = 0; i < 32; ++i)
-      if (c0 + i < p.N) acc[i] = fmaf(p.beta, Out<T>::ld(crow + c0 + i), acc[i]);
+      if (c0 + i < p.N) acc[i] = fmaf(p.beta, to_f<T>(crow[c0 + i]), acc[i]);
   }
   T o[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) o[i] = Out<T>::cvt(acc[i]);
+  for (int i = 0; i < 32; ++i) o[i] = from_f<T>(acc[i]);
   if (c0 + 31 < p.N && aligned16(drow + c0)) {
     store_row32<T>(drow + c0, o);
   } else {
@@ -282,27 +270,19 @@ __device__ __forceinline__ void epi_dispatch(const KParams& p, int b, int r, int
   }
 }
 
+using dev::pack2;
+using dev::unpack2;
+
+// True when either 16-bit value of the pair is an infinity or a NaN (all exponent bits set).
 template <typename T>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi);
-template <>
-__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
+__device__ __forceinline__ bool nonfinite_pair(uint32_t w) {
+  constexpr uint32_t E = std::is_same<T, __half>::value ? 0x7C00u : 0x7F80u;
+  return (w & E) == E || ((w >> 16) & E) == E;
 }
-template <>
-__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-template <typename T>
-__device__ __forceinline__ float unpack_lo(uint32_t w) {
-  const uint16_t b = static_cast<uint16_t>(w & 0xFFFFu);
-  return Out<T>::ld(reinterpret_cast<const T*>(&b));
-}
-template <typename T>
-__device__ __forceinline__ float unpack_hi(uint32_t w) {
-  const uint16_t b = static_cast<uint16_t>(w >> 16);
-  return Out<T>::ld(reinterpret_cast<const T*>(&b));
+
+// One lane of each warp that saw a non-finite value sets DION3_DEV_NONFINITE (warp-uniform call).
+__device__ __forceinline__ void flag_nonfinite(const KParams& p, bool bad, int lane) {
+  if (__any_sync(0xffffffffu, bad) && lane == 0 && p.status != nullptr) atomicOr(p.status, DION3_DEV_NONFINITE);
 }
 
 // 32 consecutive C values of row r starting at c0, packed in pairs (zeros where out of range).
@@ -378,6 +358,7 @@ __device__ __forceinline__ void epi_tile_tma(const KParams& p, const CUtensorMap
     ++nch;
   }
   uint32_t cnx[16];
+  bool bad = false;
   if (use_c && half < nch) load_c32<T>(p, crow, nj * BN + half * 32, cnx);
 #pragma unroll 1
   for (int ch = half; ch < nch; ch += 2) {
@@ -402,14 +383,20 @@ __device__ __forceinline__ void epi_tile_tma(const KParams& p, const CUtensorMap
       float lo = __uint_as_float(v[2 * i]) * ab;
       float hi = __uint_as_float(v[2 * i + 1]) * ab;
       if (use_c) {
-        lo = fmaf(p.beta, unpack_lo<T>(cw[i]), lo);
-        hi = fmaf(p.beta, unpack_hi<T>(cw[i]), hi);
+        const float2 c2 = unpack2<T>(cw[i]);
+        lo = fmaf(p.beta, c2.x, lo);
+        hi = fmaf(p.beta, c2.y, hi);
       }
       if (EPI == EPI_SYM && p.gamma != 0.f) {
         if (c0 + 2 * i == r) lo += p.gamma;
         if (c0 + 2 * i + 1 == r) hi += p.gamma;
       }
       w[i] = pack2<T>(lo, hi);
+    }
+    if (p.check_finite && r < p.M) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (c0 + 2 * i < p.N) bad |= nonfinite_pair<T>(c0 + 2 * i + 1 < p.N ? w[i] : (w[i] & 0xFFFFu));
     }
     const bool diag = (EPI == EPI_SYM) && (c0 == r0w);
     const bool below = (EPI == EPI_SYM) && (c0 < r0w);
@@ -461,6 +448,7 @@ __device__ __forceinline__ void epi_tile_tma(const KParams& p, const CUtensorMap
     if (tr_plain) store_block_plain(p, b, Tt, c0, r0w, lane);
     buf ^= 1;
   }
+  if (p.check_finite) flag_nonfinite(p, bad, lane);
 }
 
 // Epilogue of the fused row update W[sel[r], :] += alpha * acc.  tcgen05.ld hands each lane one
@@ -520,6 +508,7 @@ __device__ __forceinline__ void epi_tile_wupd(const KParams& p, uint8_t* stg, ui
   // Fast path: 16-byte aligned W rows, all 32 rows present; then only the chunk's columns matter.
   const bool fast = __all_sync(0xffffffffu, rows_ok) && ((p.ldw & 3) == 0) && ((p.sW & 3) == 0) && aligned16(p.W);
   float4 ring[AHEAD][8];
+  bool bad = false;
 #pragma unroll
   for (int j = 0; j < AHEAD && j < NCHW; ++j) {
     const int c0 = nj * BN + (half + j * NHALF) * 32;
@@ -566,6 +555,9 @@ __device__ __forceinline__ void epi_tile_wupd(const KParams& p, uint8_t* stg, ui
         y.z = fmaf(a.z, ab, y.z);
         y.w = fmaf(a.w, ab, y.w);
         float* w = wr[it];
+        if (w != nullptr)
+          bad |= (c < p.N && !isfinite(y.x)) || (c + 1 < p.N && !isfinite(y.y)) || (c + 2 < p.N && !isfinite(y.z)) ||
+                 (c + 3 < p.N && !isfinite(y.w));
         if (full_chunk) {
           *reinterpret_cast<float4*>(w + c) = y;
         } else if (w != nullptr) {
@@ -577,16 +569,10 @@ __device__ __forceinline__ void epi_tile_wupd(const KParams& p, uint8_t* stg, ui
       }
     }
   }
-  __syncwarp();
+  flag_nonfinite(p, bad, lane);
 }
 
-// Wait that ignores the abort flag (used while draining after an abort), bounded by time.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long limit) {
-  const long long t0 = clock64();
-  while (!ptx::mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > limit) break;
-  }
-}
+using dev::drain_wait;
 
 // ----------------------------------------------------------------------------- kernel
 template <int BN, bool B_MN, int EPI, int CL>
@@ -793,6 +779,7 @@ __global__ void __launch_bounds__(num_threads<EPI>(), 1)
         }
       }
       if (!done) {
+        bool bad = false;
 #pragma unroll 1
         for (int ch = half; ch < BN / 32; ch += 2) {
           const int c0 = nj * BN + ch * 32;
@@ -811,8 +798,13 @@ __global__ void __launch_bounds__(num_threads<EPI>(), 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) a[i] = __uint_as_float(v[i]) * ab;
             epi_dispatch<EPI>(p, b, r, c0, a);
+            if (p.check_finite) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) bad |= c0 + i < p.N && !isfinite(a[i]);
+            }
           }
         }
+        if (p.check_finite) flag_nonfinite(p, bad, lane);
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -970,6 +962,7 @@ int launch(const GemmCall& g, cudaStream_t s) {
   p.spin_limit = g.spin_limit > 0 ? g.spin_limit : DEFAULT_SPIN;
   p.eta_dev = g.eta_dev;
   p.eta_scale = g.eta_scale;
+  p.check_finite = g.check_finite ? 1 : 0;
   if (p.total_tiles == 0) return DION3_OK;
 
   CUtensorMap ta, tb;

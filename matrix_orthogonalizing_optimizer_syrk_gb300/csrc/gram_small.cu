@@ -21,6 +21,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "dev_common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -53,28 +54,8 @@ __device__ __forceinline__ uint32_t sw_off(int row, int col, int panel) {
                                ((col & 7) << 1));
 }
 
-template <typename T>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi);
-template <>
-__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-template <>
-__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-template <typename T>
-__device__ __forceinline__ float2 unpack2(uint32_t w);
-template <>
-__device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&w));
-}
-template <>
-__device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t w) {
-  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
-}
+using dev::pack2;
+using dev::unpack2;
 
 // acc = A * B over K = n16 (K-major A, MN-major B, both in the panel layout).  One thread.
 __device__ __forceinline__ void mma_nn(uint32_t d_tmem, uint32_t a_base, uint32_t b_base, int n16, int panel,
@@ -143,13 +124,7 @@ __device__ __forceinline__ void publish() {
   ptx::tc_fence_after();
 }
 
-// Bounded wait that ignores the abort flag (used while draining after an abort).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long limit) {
-  const long long t0 = clock64();
-  while (!ptx::mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > limit) break;
-  }
-}
+using dev::drain_wait;
 
 template <typename T>
 __global__ void __launch_bounds__(SEG_THREADS, 1)

@@ -55,6 +55,9 @@ struct GemmCall {
   // row update's -eta' read from device memory at run time.
   const float* eta_dev = nullptr;
   double eta_scale = 0.0;
+  // Last product of an orthogonalisation: a non-finite stored element (or updated W element)
+  // sets DION3_DEV_NONFINITE in *status.
+  bool check_finite = false;
 };
 
 // 16-bit inputs on the tcgen05 tensor cores (gemm_tc.cu).
@@ -148,6 +151,13 @@ constexpr int STEP_COL_CHUNK = 256;  // rows per partial sum of a column key
 int step_exact_limbs(int norm_p);
 // M[b][rows[b][j]][:] <- mu M[b][rows[b][j]][:] for the listed rows in [0, n).
 int step_decay_rows(int batch, int n, int m, int k, float* M, const int32_t* rows, float mu, cudaStream_t s);
+
+// Argument checks of dion3_gram_ns, in its order (api.cu).  Returns the code dion3_gram_ns would
+// return before looking at its workspace; on DION3_OK, *need is the workspace size the call needs
+// (0: nothing to do, e.g. an empty batch).
+int gram_ns_validate(int batch, int n, int m, const void* X, int64_t ldx, int64_t strideX, int x_dtype,
+                     const void* Out, int64_t ldo, int64_t strideO, int out_dtype, int T, const float* abc,
+                     const int* restart_after, int n_restart, float eps, int compute_dtype, size_t* need);
 
 // Watchdog self-test kernel (gemm_tc.cu).
 int selftest_watchdog(long long spin_limit, int* status, cudaStream_t s);

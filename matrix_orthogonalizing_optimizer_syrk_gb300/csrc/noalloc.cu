@@ -11,8 +11,11 @@
 //
 // The array's device address is looked up once per device (cudaGetSymbolAddress, with that
 // device current) by the first call made on that device, then reused; that first call should
-// come before any stream capture.  Host code never hands the array's name itself to a kernel:
-// on the host that name is a stand-in, not a device address.
+// come before any stream capture.  The saved address belongs to the device's primary context:
+// after cudaDeviceReset (which destroys that context and the library's module in it) it is no
+// longer valid, so a process that resets a device must not call this entry point on it again.
+// Host code never hands the array's name itself to a kernel: on the host that name is a
+// stand-in, not a device address.
 //
 // All calls share the one array, and it keeps whatever the last call left in it.  No part of
 // it needs to start at zero (every byte the computation reads was written earlier in the same
@@ -53,13 +56,15 @@ extern "C" int dion3_gram_ns_noalloc(int batch, int n, int m, const void* X, int
                                      int x_dtype, void* Out, int64_t ldo, int64_t strideO, int out_dtype, int T,
                                      const float* abc, const int* restart_after, int n_restart, float eps,
                                      int compute_dtype, int* status_dev, void* stream) {
-  if (batch < 0 || n < 0 || m < 0 || n > m || !dion3::dtype_valid(x_dtype) || !dion3::dtype_valid(compute_dtype))
-    return DION3_EINVAL;
-  // Reject problems that need more scratch than the array holds, before touching the GPU.
-  if (dion3_gram_ns_workspace_bytes(batch, n, m, x_dtype, compute_dtype, n_restart < 0 ? 0 : n_restart) >
-      static_cast<size_t>(DION3_NOALLOC_SCRATCH_BYTES))
-    return DION3_EWORKSPACE;
-  if (batch == 0 || n == 0) return DION3_OK;
+  // The same checks, in the same order, as dion3_gram_ns: a bad call gets the same code from
+  // both entry points.  Then problems that need more scratch than the array holds (including
+  // the copy a misaligned X needs) are rejected before the GPU is touched.
+  size_t need = 0;
+  if (int rc = dion3::gram_ns_validate(batch, n, m, X, ldx, strideX, x_dtype, Out, ldo, strideO, out_dtype, T, abc,
+                                       restart_after, n_restart, eps, compute_dtype, &need))
+    return rc;
+  if (need == 0) return DION3_OK;
+  if (need > static_cast<size_t>(DION3_NOALLOC_SCRATCH_BYTES)) return DION3_EWORKSPACE;
   void* scratch = nullptr;
   if (int rc = scratch_address(&scratch)) return rc;
   return dion3_gram_ns(batch, n, m, X, ldx, strideX, x_dtype, Out, ldo, strideO, out_dtype, T, abc, restart_after,

@@ -21,6 +21,7 @@
 
 #include <cfloat>
 
+#include "dev_common.cuh"
 #include "internal.h"
 
 namespace dion3 {
@@ -29,21 +30,9 @@ namespace {
 constexpr int SEL_THREADS = 1024;
 constexpr int MAX_N = 16384;
 
-__device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
-  const float y = __fsub_rn(x, c);
-  const float t = __fadd_rn(s, y);
-  c = __fsub_rn(__fsub_rn(t, s), y);
-  s = t;
-}
+using dev::kahan_add;
 
-template <typename T>
-__device__ __forceinline__ float gval(T v);
-template <>
-__device__ __forceinline__ float gval<float>(float v) { return v; }
-template <>
-__device__ __forceinline__ float gval<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
-template <>
-__device__ __forceinline__ float gval<__half>(__half v) { return __half2float(v); }
+using dev::to_f;
 
 template <typename T>
 __device__ __forceinline__ void load8(const T* p, float (&g)[8]) {
@@ -51,7 +40,7 @@ __device__ __forceinline__ void load8(const T* p, float (&g)[8]) {
     const uint4 u = *reinterpret_cast<const uint4*>(p);
     const T* h = reinterpret_cast<const T*>(&u);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) g[i] = gval<T>(h[i]);
+    for (int i = 0; i < 8; ++i) g[i] = to_f<T>(h[i]);
   } else {
     const float4 a = reinterpret_cast<const float4*>(p)[0];
     const float4 b = reinterpret_cast<const float4*>(p)[1];
@@ -141,7 +130,7 @@ __global__ void __launch_bounds__(256) momentum_keys_kernel(const AArgs a) {
     } else {
       for (int j = lane; j < m; j += 32) {
         const float mv = cr ? __fmul_rn(cm, Mr[j]) : Mr[j];
-        const float x = __fadd_rn(mv, gval<TG>(Gr[j]));
+        const float x = __fadd_rn(mv, to_f<TG>(Gr[j]));
         Mr[j] = x;
         q2[0] = fmaf(x, x, q2[0]);
         if (a.decay) Wr[j] = __fmul_rn(Wr[j], w_decay);

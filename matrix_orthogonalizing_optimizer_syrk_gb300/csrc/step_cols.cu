@@ -13,35 +13,16 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "dev_common.cuh"
 #include "internal.h"
 
 namespace dion3 {
 namespace {
 
-__device__ __forceinline__ void kahan(float& s, float& c, float x) {
-  const float y = __fsub_rn(x, c);
-  const float t = __fadd_rn(s, y);
-  c = __fsub_rn(__fsub_rn(t, s), y);
-  s = t;
-}
+using dev::kahan_add;
 
-template <typename T>
-__device__ __forceinline__ float to_f(T v);
-template <>
-__device__ __forceinline__ float to_f<float>(float v) { return v; }
-template <>
-__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
-template <>
-__device__ __forceinline__ float to_f<__half>(__half v) { return __half2float(v); }
-
-template <typename T>
-__device__ __forceinline__ T from_f(float v);
-template <>
-__device__ __forceinline__ float from_f<float>(float v) { return v; }
-template <>
-__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
-template <>
-__device__ __forceinline__ __half from_f<__half>(float v) { return __float2half_rn(v); }
+using dev::from_f;
+using dev::to_f;
 
 struct ColA {
   int m, n, nchunk;
@@ -93,7 +74,7 @@ __global__ void __launch_bounds__(256) colkeys_kernel(const ColA a) {
       q2 = fmaf(v, v, q2);
       if (a.keys) {
         bad |= !isfinite(v);
-        kahan(s, comp, NORM_P == 1 ? fabsf(v) : __fmul_rn(v, v));
+        kahan_add(s, comp, NORM_P == 1 ? fabsf(v) : __fmul_rn(v, v));
       }
     }
   }

@@ -113,6 +113,50 @@ def test_gram_ns_validation(L):
     assert _gram(L, abc=nan_abc) == 1
 
 
+def _gram_pair(L, batch=1, n=64, m=128, X=FAKE, ldx=128, Out=FAKE, ldo=128, T=5, abc=None, rs=(2,), xt=0, ot=0,
+               ct=0, eps=1e-7, wsb=1 << 40):
+    """The same call through dion3_gram_ns (ample fake workspace) and dion3_gram_ns_noalloc."""
+    abc = _abc(T) if abc is None else abc
+    r = (ctypes.c_int * max(1, len(rs)))(*rs)
+    a = L.dion3_gram_ns(batch, n, m, X, ldx, n * ldx, xt, Out, ldo, n * ldo, ot, T, abc, r, len(rs), eps, ct,
+                        FAKE, wsb, NULL, NULL)
+    b = L.dion3_gram_ns_noalloc(batch, n, m, X, ldx, n * ldx, xt, Out, ldo, n * ldo, ot, T, abc, r, len(rs), eps,
+                                ct, NULL, NULL)
+    return a, b
+
+
+def test_noalloc_returns_the_same_codes_as_the_workspace_entry_point(L):
+    """Bad and empty calls get the same code from both Gram NS entry points (nothing reaches the
+    GPU: every case fails or finishes in the argument checks)."""
+    nan_abc = (ctypes.c_float * 15)(*([float("nan")] * 15))
+    cases = [dict(n=200, m=100, ldx=100, ldo=104), dict(T=0), dict(rs=(0,)), dict(rs=(5,)), dict(rs=(3, 2)),
+             dict(X=NULL), dict(Out=NULL), dict(eps=-1.0), dict(Out=FAKE_ODD), dict(ct=2, ot=0), dict(abc=nan_abc),
+             dict(xt=7), dict(ct=9), dict(ldx=100), dict(batch=-1),
+             # empty problems: OK from both, even with a bad schedule or dtype left unchecked by neither
+             dict(batch=0), dict(n=0), dict(batch=0, n=200, m=100), dict(batch=0, T=0), dict(batch=0, ct=2, ot=0)]
+    for kw in cases:
+        a, b = _gram_pair(L, **kw)
+        assert a == b, f"{kw}: dion3_gram_ns -> {a}, dion3_gram_ns_noalloc -> {b}"
+        assert a != 3, kw
+
+
+def test_noalloc_rejects_oversized_problems_on_the_host(L):
+    """Beyond DION3_NOALLOC_SCRATCH_BYTES: DION3_EWORKSPACE before the GPU is touched -- also when
+    only the copy that a misaligned X needs pushes the workspace over the limit."""
+    cap = d3.NOALLOC_SCRATCH_BYTES
+    assert _gram_pair(L, batch=8, n=1024, m=4096, ldx=4096, ldo=4096, rs=(2, 4))[1] == 3
+    # find an aligned problem that fits, whose copied (misaligned-X) variant does not
+    n, m = 512, 4096
+    batch = 1
+    while d3.workspace_bytes_gram_ns(batch + 1, n, m, 0, 0, 1) <= cap:
+        batch += 1
+    fits = d3.workspace_bytes_gram_ns(batch, n, m, 0, 0, 1)
+    copied = d3.workspace_bytes_gram_ns(batch, n, m, 0, 1, 1)   # bf16 X, fp16 compute: copied
+    assert fits <= cap < copied
+    assert _gram_pair(L, batch=batch, n=n, m=m, ldx=m, ldo=m, X=FAKE_ODD, rs=(2,))[1] == 3
+    assert _gram_pair(L, batch=batch, n=n, m=m, ldx=m, ldo=m, xt=0, ct=1, rs=(2,))[1] == 3
+
+
 def test_workspace_queries(L):
     small = d3.workspace_bytes_gram_ns(1, 64, 128, 0, 0, 1)
     big = d3.workspace_bytes_gram_ns(2, 64, 128, 0, 0, 1)
