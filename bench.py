@@ -62,7 +62,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sub", action="store_true", help="skip the Gram-NS and sym-GEMM sub-measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
-    ap.add_argument("--case", choices=["gram_small", "step_small", "sym_gemm", "moe", "moe_gram", "moe_w2_cols", "fp32"],
+    ap.add_argument("--case", choices=["gram_small", "gram_mid", "gram_mid_mlp", "step_small", "sym_gemm", "sym_small",
+                                       "moe", "moe_gram", "moe_w2_cols", "fp32"],
                     default=None,
                     help="run one small profiling case (a few GB, inputs larger than L2) instead of the bench")
     return ap.parse_args()
@@ -842,6 +843,16 @@ def run_case(args):
         B, n, m = 16, 1024, 4096  # 128 MB of bf16 input
         X = synthetic.lowrank_batch(B, n, m, base_seed=7000, dtype=torch.bfloat16, device=dev)
         fn = lambda: d3.gram_ns(X, ABC, RESTARTS, compute=torch.float16)  # noqa: E731
+    elif args.case in ("gram_mid", "gram_mid_mlp"):
+        # the 7B step's product chain on 72 of its selected-row matrices (k = 1024, fp16 X_S read in
+        # place): every launch's working set is larger than L2 (each k x k buffer 144 MB), so its
+        # DRAM bytes per matrix carry over to the full megabatches (ncu traffic captures)
+        B, n, m = 72, 1024, (4096 if args.case == "gram_mid" else 11008)
+        X = synthetic.lowrank_batch(B, n, m, base_seed=7050, dtype=torch.float16, device=dev)
+        O = torch.empty_like(X)
+        ws = torch.empty(d3.workspace_bytes_gram_ns(B, n, m, torch.float16, torch.float16, len(RESTARTS)),
+                         dtype=torch.uint8, device=dev)
+        fn = lambda: d3.gram_ns(X, ABC, RESTARTS, compute=torch.float16, out=O, workspace=ws)  # noqa: E731
     elif args.case == "step_small":
         B, n, m = 16, 4096, 4096  # 1 GB of W and of M, 0.5 GB of G
         W = synthetic.gaussian((B, n, m), seed=7100, std=0.02, device=dev)
@@ -866,6 +877,30 @@ def run_case(args):
         M = torch.zeros((B, m, n), dtype=torch.float32, device=dev)
         G = synthetic.lowrank_batch(B, m, n, base_seed=7800, dtype=torch.bfloat16, device=dev)
         fn = lambda: d3.step_cols(W, M, G, f=(1, 8), mu=MU, eta=ETA, abc=ABC, restart_after=RESTARTS)  # noqa: E731
+    elif args.case == "sym_small":
+        # the small corner of the symmetric-GEMM sweep, each shape ours then torch.matmul (cuBLAS),
+        # with a 256 MB L2 flush before every call
+        flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        calls = []
+        for n, k in ((1024, 1024), (1024, 4096), (2048, 2048), (2048, 8192)):
+            A = synthetic.gaussian((n, k), seed=2000 + n + k, std=k ** -0.5, dtype=torch.bfloat16, device=dev)
+            D = torch.empty((n, n), dtype=torch.bfloat16, device=dev)
+            calls.append((f"{n}x{k}", A, D))
+
+        def fn():
+            for _, A, D in calls:
+                flush_buf.fill_(1)
+                d3.sym_gemm(A, out=D)
+                flush_buf.fill_(1)
+                torch.matmul(A, A.T, out=D)
+        for name, A, D in calls:
+            ours = lambda: d3.sym_gemm(A, out=D)  # noqa: E731
+            ref = lambda: torch.matmul(A, A.T, out=D)  # noqa: E731
+            ours()
+            ref()
+            torch.cuda.synchronize()
+            out[name] = {"ours_us": 1e3 * _time_calls(torch, ours, 10, lambda: flush_buf.fill_(1)),
+                         "torch_matmul_us": 1e3 * _time_calls(torch, ref, 10, lambda: flush_buf.fill_(1))}
     elif args.case == "fp32":
         X = synthetic.gaussian((256, 1024), seed=0, device="cpu").to(dev)
         fn = lambda: d3.gram_ns(X, ABC, (2,), compute=torch.float32)  # noqa: E731

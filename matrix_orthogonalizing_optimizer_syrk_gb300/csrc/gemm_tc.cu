@@ -22,6 +22,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -868,10 +869,71 @@ EncodeFn get_encode() {
   return fn;
 }
 
+// Encoded maps are a pure function of their arguments; a product chain encodes the same few
+// again and again, so the last ones are kept (direct-mapped on a hash of the arguments).
+struct MapKey {
+  const void* ptr;
+  int64_t ld, stride;
+  int dtype, rows, cols, batch, box_cols, box_rows, swz;
+};
+
+bool same_key(const MapKey& a, const MapKey& b) {
+  return a.ptr == b.ptr && a.ld == b.ld && a.stride == b.stride && a.dtype == b.dtype && a.rows == b.rows &&
+         a.cols == b.cols && a.batch == b.batch && a.box_cols == b.box_cols && a.box_rows == b.box_rows &&
+         a.swz == b.swz;
+}
+
+constexpr int MAP_CACHE = 256;
+struct MapCache {
+  std::mutex mu;
+  bool used[MAP_CACHE] = {};
+  MapKey key[MAP_CACHE];
+  CUtensorMap map[MAP_CACHE];
+};
+MapCache& map_cache() {
+  static MapCache c;
+  return c;
+}
+
+size_t key_slot(const MapKey& k) {
+  uint64_t h = 1469598103934665603ull;
+  auto mix = [&](uint64_t v) { h = (h ^ v) * 1099511628211ull; };
+  mix(reinterpret_cast<uintptr_t>(k.ptr));
+  mix(static_cast<uint64_t>(k.ld));
+  mix(static_cast<uint64_t>(k.stride));
+  mix((static_cast<uint64_t>(k.rows) << 32) ^ static_cast<uint32_t>(k.cols));
+  mix((static_cast<uint64_t>(k.batch) << 32) ^ static_cast<uint32_t>(k.box_cols * 4096 + k.box_rows));
+  mix(static_cast<uint64_t>(k.dtype * 16 + k.swz));
+  return static_cast<size_t>(h % MAP_CACHE);
+}
+
+bool encode_map(CUtensorMap* map, const Mat& m, int rows, int cols, int batch, int box_cols, int box_rows,
+                CUtensorMapSwizzle swz);
+
 // 3-D map over a 16-bit [batch][rows][cols] operand, box = box_cols x box_rows, 128-byte swizzle
 // (operand loads) or 64-byte swizzle (32 x 32 epilogue stores).
 bool make_map(CUtensorMap* map, const Mat& m, int rows, int cols, int batch, int box_cols, int box_rows,
               CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+  const MapKey k{m.ptr, m.ld, m.stride, m.dtype, rows, cols, batch, box_cols, box_rows, static_cast<int>(swz)};
+  const size_t slot = key_slot(k);
+  MapCache& c = map_cache();
+  {
+    std::lock_guard<std::mutex> lock(c.mu);
+    if (c.used[slot] && same_key(c.key[slot], k)) {
+      *map = c.map[slot];
+      return true;
+    }
+  }
+  if (!encode_map(map, m, rows, cols, batch, box_cols, box_rows, swz)) return false;
+  std::lock_guard<std::mutex> lock(c.mu);
+  c.used[slot] = true;
+  c.key[slot] = k;
+  c.map[slot] = *map;
+  return true;
+}
+
+bool encode_map(CUtensorMap* map, const Mat& m, int rows, int cols, int batch, int box_cols, int box_rows,
+                CUtensorMapSwizzle swz) {
   EncodeFn enc = get_encode();
   if (!enc) return false;
   const cuuint64_t es = 2;
@@ -987,8 +1049,15 @@ int launch(const GemmCall& g, cudaStream_t s) {
     if (!make_map(&td, g.D, g.M, g.N, g.batch, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return DION3_ECUDA;
   }
   auto kern = tc_gemm_kernel<BN, B_MN, EPI, CL>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM) != cudaSuccess)
-    return DION3_ECUDA;
+  // The shared-memory opt-in is set once per device for each instantiation.
+  static std::atomic<bool> smem_set[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DION3_ECUDA;
+  if (dev < 0 || dev >= 64 || !smem_set[dev].load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM) != cudaSuccess)
+      return DION3_ECUDA;
+    if (dev >= 0 && dev < 64) smem_set[dev].store(true, std::memory_order_release);
+  }
   if constexpr (CL == 1) {
     long long grid = sm_count();
     if (grid > p.total_tiles) grid = p.total_tiles;
