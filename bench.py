@@ -62,8 +62,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sub", action="store_true", help="skip the Gram-NS and sym-GEMM sub-measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
-    ap.add_argument("--case", choices=["gram_small", "gram_mid", "gram_mid_mlp", "step_small", "sym_gemm", "sym_small",
-                                       "moe", "moe_gram", "moe_w2_cols", "fp32"],
+    ap.add_argument("--case", choices=["gram_small", "gram_mid", "gram_mid_mlp", "step_small", "step_small_mlp",
+                                       "sym_gemm", "sym_small", "moe", "moe_gram", "moe_w2_cols", "fp32"],
                     default=None,
                     help="run one small profiling case (a few GB, inputs larger than L2) instead of the bench")
     return ap.parse_args()
@@ -853,8 +853,9 @@ def run_case(args):
         ws = torch.empty(d3.workspace_bytes_gram_ns(B, n, m, torch.float16, torch.float16, len(RESTARTS)),
                          dtype=torch.uint8, device=dev)
         fn = lambda: d3.gram_ns(X, ABC, RESTARTS, compute=torch.float16, out=O, workspace=ws)  # noqa: E731
-    elif args.case == "step_small":
-        B, n, m = 16, 4096, 4096  # 1 GB of W and of M, 0.5 GB of G
+    elif args.case in ("step_small", "step_small_mlp"):
+        # 16 x 4096 x 4096 (1 GB of W and of M, 0.5 GB of G) or 8 x 4096 x 11008 (1.4 GB of W and of M)
+        B, n, m = (16, 4096, 4096) if args.case == "step_small" else (8, 4096, 11008)
         W = synthetic.gaussian((B, n, m), seed=7100, std=0.02, device=dev)
         M = torch.zeros((B, n, m), dtype=torch.float32, device=dev)
         G = synthetic.lowrank_batch(B, n, m, base_seed=7200, dtype=torch.bfloat16, device=dev)
