@@ -67,6 +67,11 @@ typedef enum { DION3_BF16 = 0, DION3_FP16 = 1, DION3_FP32 = 2 } dion3_dtype;
 #define DION3_DEV_TIMEOUT   0x2 /* a bounded wait gave up; outputs of that call are undefined */
 #define DION3_DEV_SELECT    0x4 /* row selection could not certify k rows (internal error), or a
                                    caller-chosen S was not k distinct ascending rows in [0, n) */
+#define DION3_DEV_RANGE     0x8 /* checked builds only (libdion3_checked.so, see dion3_range_checks):
+                                   a kernel found an index outside its buffer -- a selected or
+                                   carried row outside [-1, n), or a tile outside its matrix -- and
+                                   skipped the access.  -1 is the blank a failed selection leaves
+                                   and is not flagged. */
 
 /*
  * dion3_sym_gemm -- D = alpha * A * B^T + beta * C + gamma * I, for results known to be
@@ -401,6 +406,15 @@ const char* dion3_status_str(int code);
 
 /* DION3_ABI_VERSION of the loaded library. */
 int dion3_abi_version(void);
+
+/*
+ * dion3_range_checks -- 1 if this library was built with in-kernel range checks
+ * (libdion3_checked.so: every entry point above, same arguments and results, plus
+ * DION3_DEV_RANGE in *status_dev when an index leaves its buffer), 0 for the default build.
+ * The checked build stands in for a memory checker, which the GPUs this library is tested on
+ * do not offer; it never traps.  No counterpart on the pages.
+ */
+int dion3_range_checks(void);
 
 /*
  * dion3_selftest_watchdog -- diagnostic for the bounded-wait machinery (no counterpart on the

@@ -26,9 +26,11 @@ import torch
 
 _DIR = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_DIR, "libdion3.so")
+# The same library built with in-kernel range checks (DION3_DEV_RANGE); see use_checked_build().
+CHECKED_LIB_PATH = os.path.join(_DIR, "libdion3_checked.so")
 
 BF16, FP16, FP32 = 0, 1, 2
-DEV_NONFINITE, DEV_TIMEOUT, DEV_SELECT = 0x1, 0x2, 0x4
+DEV_NONFINITE, DEV_TIMEOUT, DEV_SELECT, DEV_RANGE = 0x1, 0x2, 0x4, 0x8
 _DT = {torch.bfloat16: BF16, torch.float16: FP16, torch.float32: FP32}
 
 _c_int, _c_i64, _c_f, _c_p, _c_sz = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
@@ -73,12 +75,14 @@ SIGNATURES = {
                                        _c_int, _c_p, _c_p]),
     "dion3_status_str": (ctypes.c_char_p, [_c_int]),
     "dion3_abi_version": (_c_int, []),
+    "dion3_range_checks": (_c_int, []),
     "dion3_selftest_watchdog": (_c_int, [ctypes.c_longlong, _c_p, _c_p]),
 }
 
 SELECT_GIVEN = 0  # norm_p of a caller-chosen row set (DION3_SELECT_GIVEN)
 
 _lib = None
+_lib_path = LIB_PATH
 
 
 class Dion3Error(RuntimeError):
@@ -87,14 +91,26 @@ class Dion3Error(RuntimeError):
         super().__init__(f"{where}: {status_str(code)} ({code})")
 
 
+def use_checked_build() -> None:
+    """Load libdion3_checked.so instead of libdion3.so (call before the first entry point).
+
+    The checked build runs the same kernels with in-kernel range checks that set DEV_RANGE in
+    the status word; it is built by ``_build.build(checked=True)``.
+    """
+    global _lib_path
+    if _lib is not None and _lib_path != CHECKED_LIB_PATH:
+        raise RuntimeError("the default library is already loaded in this process")
+    _lib_path = CHECKED_LIB_PATH
+
+
 def lib() -> ctypes.CDLL:
-    """The loaded libdion3.so (raises if it has not been built)."""
+    """The loaded library (raises if it has not been built)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing; build it with "
+        if not os.path.exists(_lib_path):
+            raise RuntimeError(f"{_lib_path} is missing; build it with "
                                "`python -m matrix_orthogonalizing_optimizer_syrk_gb300._build`")
-        L = ctypes.CDLL(LIB_PATH)
+        L = ctypes.CDLL(_lib_path)
         for name, (res, args) in SIGNATURES.items():
             fn = getattr(L, name)
             fn.restype = res

@@ -307,6 +307,11 @@ extern "C" {
 
 int dion3_abi_version(void) { return DION3_ABI_VERSION; }
 
+#ifndef DION3_RANGE_CHECKS
+#define DION3_RANGE_CHECKS 0
+#endif
+int dion3_range_checks(void) { return DION3_RANGE_CHECKS; }
+
 const char* dion3_status_str(int code) {
   switch (code) {
     case DION3_OK:

@@ -7,10 +7,28 @@
 
 #include <cstdint>
 
+#include "dion3.h"
 #include "ptx.cuh"
+
+// Checked builds (libdion3_checked.so) compile with DION3_RANGE_CHECKS=1: the index checks below
+// then set DION3_DEV_RANGE in the caller's status word.  In the default build they compile to
+// nothing; the accesses they guard are skipped by the kernels' own bounds in both builds.
+#ifndef DION3_RANGE_CHECKS
+#define DION3_RANGE_CHECKS 0
+#endif
 
 namespace dion3 {
 namespace dev {
+
+// An index that should lie in its buffer: `ok` false sets DION3_DEV_RANGE (checked builds only).
+__device__ __forceinline__ void range_check(bool ok, int* status) {
+#if DION3_RANGE_CHECKS
+  if (!ok && status != nullptr) atomicOr(status, DION3_DEV_RANGE);
+#else
+  (void)ok;
+  (void)status;
+#endif
+}
 
 // Conversions between a stored element type (fp32, bf16, fp16) and fp32, round to nearest.
 template <typename T>

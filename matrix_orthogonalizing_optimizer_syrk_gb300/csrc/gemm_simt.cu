@@ -6,6 +6,7 @@
 // shared memory, the next K block being loaded into registers while the current one is used,
 // so global-load latency is hidden behind the FMAs.  This path serves the 1e-4 parity mode;
 // the 16-bit path is the fast one.
+#include "dev_common.cuh"
 #include "internal.h"
 
 namespace dion3 {
@@ -145,6 +146,7 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SParams p) {
         bad |= !isfinite(v);
       } else {
         const int row = p.sel[static_cast<long long>(b) * p.ssel + r];
+        dev::range_check(row >= -1 && row < p.w_rows, p.status);
         if (row < 0 || row >= p.w_rows) continue;
         float* w = p.W + static_cast<long long>(b) * p.sW + static_cast<long long>(row) * p.ldw + c;
         const float nw = *w + v;

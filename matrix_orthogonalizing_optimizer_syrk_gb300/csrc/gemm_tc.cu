@@ -52,10 +52,9 @@ struct Cfg {
   static constexpr int EPIW = epi_warps<EPI>();
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = (BN / CL) * BK * 2;
-  // Epilogue staging per warp: one {32x32 block, its transpose} in 16 bits (stored products), or
-  // one 32 x 36 fp32 block and 32 row pointers (W row update).  One staging buffer instead of two
-  // leaves room for a sixth operand stage (measured: 1% faster product chain, 3% on large SYRK).
-  static constexpr int STG_WARP = EPI == EPI_WUPD ? 5120 : 2 * 2048;
+  // Epilogue staging per warp: two buffers of {32x32 block, its transpose} in 16 bits (stored
+  // products), or one 32 x 36 fp32 block and 32 row pointers (W row update).
+  static constexpr int STG_WARP = EPI == EPI_WUPD ? 5120 : 2 * 2 * 2048;
   static constexpr int STAGE_BUDGET = 232448 - EPIW * STG_WARP - 2048;  // 227 KB minus staging and barriers
   static constexpr int STAGES = (STAGE_BUDGET / (A_BYTES + B_BYTES)) < 8 ? (STAGE_BUDGET / (A_BYTES + B_BYTES)) : 8;
   static constexpr int STG_OFF = STAGES * (A_BYTES + B_BYTES);
@@ -232,6 +231,7 @@ __device__ __forceinline__ void epi_gen(const KParams& p, int b, int r, int c0, 
 
 __device__ __forceinline__ void epi_wupd(const KParams& p, int b, int r, int c0, const float (&acc)[32]) {
   const int row = __ldg(p.sel + static_cast<long long>(b) * p.ssel + r);
+  dev::range_check(row >= -1 && row < p.w_rows, p.status);
   if (row < 0 || row >= p.w_rows) return;  // only after a failed selection
   float* wrow = p.W + static_cast<long long>(b) * p.sW + static_cast<long long>(row) * p.ldw;
   if (c0 + 31 < p.N && aligned16(wrow + c0)) {
@@ -344,7 +344,7 @@ __device__ __noinline__ void store_block_plain(const KParams& p, int b, const ui
 // Chunks whose columns lie entirely above the warp's rows are skipped; TMA clips rows and
 // columns outside the matrix, and a warp whose rows all lie outside stores nothing.
 template <typename T, int BN, int EPI>
-__device__ __forceinline__ void epi_tile_tma(const KParams& p, const CUtensorMap* tmD, uint8_t* stg,
+__device__ __forceinline__ void epi_tile_tma(const KParams& p, const CUtensorMap* tmD, uint8_t* stg, int& buf,
                                              uint32_t t_acc, int b, int mi, int nj, int ew, int half, int lane,
                                              float ab) {
   const int r0w = mi * BM + ew * 32;
@@ -402,10 +402,10 @@ __device__ __forceinline__ void epi_tile_tma(const KParams& p, const CUtensorMap
     }
     const bool diag = (EPI == EPI_SYM) && (c0 == r0w);
     const bool below = (EPI == EPI_SYM) && (c0 < r0w);
-    // the previous chunk's TMA stores must have read the staging buffer
-    if (lane == 0) ptx::bulk_wait_read_0();
+    // the buffer used two chunks ago must have been read by its TMA store
+    if (lane == 0) ptx::bulk_wait_read_le1();
     __syncwarp();
-    uint8_t* S = stg;
+    uint8_t* S = stg + buf * 4096;
     uint8_t* Tt = S + 2048;
 #pragma unroll
     for (int q = 0; q < 4; ++q)
@@ -448,6 +448,7 @@ __device__ __forceinline__ void epi_tile_tma(const KParams& p, const CUtensorMap
     }
     if (blk_plain) store_block_plain(p, b, S, r0w, c0, lane);
     if (tr_plain) store_block_plain(p, b, Tt, c0, r0w, lane);
+    buf ^= 1;
   }
   if (p.check_finite) flag_nonfinite(p, bad, lane);
 }
@@ -490,6 +491,7 @@ __device__ __forceinline__ void epi_tile_wupd(const KParams& p, uint8_t* stg, ui
     float* wrow = nullptr;
     if (r < p.M) {
       const int row = __ldg(p.sel + static_cast<long long>(b) * p.ssel + r);
+      dev::range_check(row >= -1 && row < p.w_rows, p.status);
       if (row >= 0 && row < p.w_rows)  // only a failed selection leaves rows outside [0, w_rows)
         wrow = p.W + static_cast<long long>(b) * p.sW + static_cast<long long>(row) * p.ldw;
     }
@@ -643,6 +645,11 @@ __global__ void __launch_bounds__(num_threads<EPI>(), 1)
       for (long long t = unit0; ok && t < p.total_tiles; t += unit_step) {
         int b, mi, nj;
         decode_tile<EPI, BN, CL>(p, t, rank, b, mi, nj);
+        // the tile scheduler's invariants: a matrix of the batch, a row block of the (pair-rounded)
+        // row grid, a column block of the column grid (and at or below the diagonal for SYM)
+        dev::range_check(b >= 0 && b < p.batch && mi >= 0 && mi < (p.tiles_m + CL - 1) / CL * CL && nj >= 0 &&
+                             nj < p.tiles_n && (EPI != EPI_SYM || nj * BN <= mi * BM + BM - 1),
+                         p.status);
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!ptx::mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort, lim)) {
             ok = false;
@@ -752,6 +759,7 @@ __global__ void __launch_bounds__(num_threads<EPI>(), 1)
     const int ew = warp & 3;  // TMEM lanes 32*ew .. 32*ew+31
     const int half = (warp - 2) >> 2;  // the two warps of a lane quarter split the chunks
     uint8_t* stg = smem + Cf::STG_OFF + (warp - 2) * Cf::STG_WARP;
+    int buf = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (long long t = unit0; t < p.total_tiles; t += unit_step) {
@@ -772,9 +780,9 @@ __global__ void __launch_bounds__(num_threads<EPI>(), 1)
       } else {
         if (p.d_type != FP32) {
           if (p.d_type == FP16)
-            epi_tile_tma<__half, BN, EPI>(p, &tmD, stg, t_acc, b, mi, nj, ew, half, lane, ab);
+            epi_tile_tma<__half, BN, EPI>(p, &tmD, stg, buf, t_acc, b, mi, nj, ew, half, lane, ab);
           else
-            epi_tile_tma<__nv_bfloat16, BN, EPI>(p, &tmD, stg, t_acc, b, mi, nj, ew, half, lane, ab);
+            epi_tile_tma<__nv_bfloat16, BN, EPI>(p, &tmD, stg, buf, t_acc, b, mi, nj, ew, half, lane, ab);
           done = true;
         }
       }

@@ -281,6 +281,7 @@ __device__ void selected_scale(const BArgs& a, int b, const int32_t* sel) {
   double acc = 0.0;
   for (int j = lane; j < a.k; j += 32) {
     const int i = sel[j];
+    dev::range_check(i >= -1 && i < a.n, a.status);
     if (i >= 0 && i < a.n) acc += static_cast<double>(rq[i]);
   }
 #pragma unroll
@@ -468,6 +469,7 @@ struct CArgs {
   const float* mu_dev;  // when set, mu is read from here
   const float* scale;
   float* mu_out;  // when set, the mu of this step is stored here (a decay left pending)
+  int* status;
 };
 
 template <typename T>
@@ -491,6 +493,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const CArgs a) {
     const long long b = row / a.k;
     const int i = a.sel[row];
     TC* dst = static_cast<TC*>(a.XS) + row * a.ldx;
+    dev::range_check(i >= -1 && i < a.n, a.status);  // -1: the blank left by a failed selection
     if (i < 0 || i >= a.n) {  // only after a failed selection (DION3_DEV_SELECT is set)
       for (int c = lane; c < a.m; c += 32) dst[c] = cvt_out<TC>(0.f);
       continue;
@@ -567,7 +570,8 @@ int launch_c(const CArgs& c, bool vec, bool write_m, cudaStream_t s) {
 
 // Carried decay, flag pass: flag[b][i] = 1 for the listed rows of matrix b, 0 elsewhere.  One CTA
 // per matrix; entries outside [0, n) (the -1 of a failed selection) list nothing.
-__global__ void __launch_bounds__(256) carry_flags_kernel(int n, int k, const int32_t* rows, uint8_t* flag) {
+__global__ void __launch_bounds__(256) carry_flags_kernel(int n, int k, const int32_t* rows, uint8_t* flag,
+                                                          int* status) {
   const int b = blockIdx.x;
   uint8_t* f = flag + static_cast<long long>(b) * n;
   for (int i = threadIdx.x; i < n; i += blockDim.x) f[i] = 0;
@@ -575,6 +579,7 @@ __global__ void __launch_bounds__(256) carry_flags_kernel(int n, int k, const in
   const int32_t* r = rows + static_cast<long long>(b) * k;
   for (int j = threadIdx.x; j < k; j += blockDim.x) {
     const int i = r[j];
+    dev::range_check(i >= -1 && i < n, status);
     if (i >= 0 && i < n) f[i] = 1;
   }
 }
@@ -631,7 +636,7 @@ int step_momentum_keys(const StepArgs& s, cudaStream_t st) {
   a.carry_mu_dev = s.carry_mu_dev;
   if (a.rows == 0) return DION3_OK;
   if (a.carry != nullptr) {
-    carry_flags_kernel<<<s.batch, 256, 0, st>>>(s.n, s.k, s.carry_rows, s.carry_flag);
+    carry_flags_kernel<<<s.batch, 256, 0, st>>>(s.n, s.k, s.carry_rows, s.carry_flag, s.status);
     if (cudaGetLastError() != cudaSuccess) return DION3_ECUDA;
   }
   const bool vec = (s.m % 8 == 0) && aligned16(s.M) && aligned16(s.G) && aligned16(s.W);
@@ -698,6 +703,7 @@ int step_gather(const StepArgs& s, cudaStream_t st) {
   c.mu_dev = s.hyper;
   c.scale = s.scale;
   c.mu_out = s.defer ? s.carry_mu_dev : nullptr;
+  c.status = s.status;
   const bool vec = (s.m % 4 == 0) && aligned16(s.M) && (s.ldx % 8 == 0);
   switch (s.cdt) {
     case FP32:

@@ -142,6 +142,7 @@ struct ColC {
   float mu;
   const float* mu_dev;
   const float* scale;
+  int* status;
 };
 
 // Pass C: a block of 32 rows; 8 warps.  Lanes over 32 selected columns read M[i][S_j] (and
@@ -160,6 +161,7 @@ __global__ void __launch_bounds__(256) gather_cols_kernel(const ColC a) {
   for (int jc = 0; jc < a.k; jc += 32) {
     const int j = jc + lane;
     const int col = j < a.k ? sel[j] : -1;
+    dev::range_check(col >= -1 && col < a.n, a.status);
     const bool ok = col >= 0 && col < a.n;  // -1 only after a failed selection
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) {
@@ -191,6 +193,7 @@ struct ColU {
   float alpha;
   const float* eta_dev;
   double eta_scale;
+  int* status;
 };
 
 // W update: lanes over 32 rows read O[j][i] (coalesced), the tile is transposed, lanes over 32
@@ -215,6 +218,7 @@ __global__ void __launch_bounds__(256) scatter_cols_kernel(const ColU a) {
     __syncthreads();
     const int j = jc + lane;
     const int col = j < a.k ? sel[j] : -1;
+    dev::range_check(col >= -1 && col < a.n, a.status);
     const bool ok = col >= 0 && col < a.n;
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) {
@@ -301,6 +305,7 @@ int step_gather_cols(const StepArgs& s, cudaStream_t st) {
   c.mu = s.mu;
   c.mu_dev = s.hyper;
   c.scale = s.scale;
+  c.status = s.status;
   const dim3 grid(static_cast<unsigned>((s.m + 31) / 32), static_cast<unsigned>(s.batch));
   switch (s.cdt) {
     case FP32:
@@ -331,6 +336,7 @@ int step_scatter_cols(const StepArgs& s, const void* O, int64_t ldo, float alpha
   u.alpha = alpha;
   u.eta_dev = eta_dev;
   u.eta_scale = eta_scale;
+  u.status = s.status;
   const dim3 grid(static_cast<unsigned>((s.m + 31) / 32), static_cast<unsigned>(s.batch));
   switch (s.cdt) {
     case FP32:

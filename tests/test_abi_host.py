@@ -364,3 +364,19 @@ def test_binding_signatures_match_header():
         assert len(args) == len(params), f"{name}: header has {len(params)} parameters, binding {len(args)}"
         for i, (p, a) in enumerate(zip(params, args)):
             assert _decl_kind(p) == _ctype_kind(a), f"{name} argument {i} ({p}): binding declares {a}"
+
+
+def test_checked_build_loads_and_reports_itself():
+    """The range-checked variant (DION3_RANGE_CHECKS=1) exports the same symbols and reports 1 from
+    dion3_range_checks; the default build reports 0."""
+    path = _build.build(checked=True)
+    assert path.endswith("libdion3_checked.so")
+    Lc = ctypes.CDLL(path)
+    for name in _declared_functions():
+        assert hasattr(Lc, name), f"libdion3_checked.so does not export {name}"
+    Lc.dion3_range_checks.restype = ctypes.c_int
+    assert Lc.dion3_range_checks() == 1
+    assert d3.lib().dion3_range_checks() == 0
+    # argument validation is the same code in both builds
+    Lc.dion3_k.restype = ctypes.c_int
+    assert Lc.dion3_k(4096, 1, 4) == 1024
