@@ -137,24 +137,23 @@ def clock_at_max(clk) -> bool:
         return False
 
 
-def time_l2_steps(torch, d3, mbs, ws, status, args, K):
-    """K carried steps of both megabatches with rows ranked by the exact sum of squares (L2)."""
+def time_variant_steps(torch, d3, mbs, ws, status, K, workload, **kw):
+    """K carried steps of both megabatches with one option changed (same state chain)."""
     if K <= 0:
         return None
-    for s in range(2):   # the first L2 step applies the last L1 step's pending decay
+    for s in range(2):   # the first step applies the previous variant's pending decay
         for x in mbs:
-            carried_step(d3, x, s % 2, ws, status, norm_p=2)
+            carried_step(d3, x, s % 2, ws, status, **kw)
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record()
     for s in range(K):
         for x in mbs:
-            carried_step(d3, x, s % 2, ws, status, norm_p=2)
+            carried_step(d3, x, s % 2, ws, status, **kw)
     t1.record()
     torch.cuda.synchronize()
-    return {"workload": "the headline step with norm_p=2 (rows ranked by exact sums of squares, i.e. by row L2 "
-                        "norm), same megabatches and state chain", "ms_per_step": t0.elapsed_time(t1) / K,
-            "steps": K, "device_status": int(status.item())}
+    return {"workload": workload, "ms_per_step": t0.elapsed_time(t1) / K, "steps": K,
+            "device_status": int(status.item())}
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -245,12 +244,13 @@ def step_inputs(torch, synthetic, dev, rank: int):
     return mbs
 
 
-def carried_step(d3, x, slot, ws, status, events=None, f=F, norm_p=1):
+def carried_step(d3, x, slot, ws, status, events=None, f=F, norm_p=1, compute=None):
     """One step of megabatch x; its decay of M[S,:] is left to the next call (x["carried"])."""
     import torch
 
     d3.step(x["W"], x["M"], x["Gs"][slot], f=f, mu=MU, eta=ETA, norm_p=norm_p, abc=ABC, restart_after=RESTARTS,
-            compute=torch.float16, sel_out=x["sel"], workspace=ws, status=status, events=events,
+            compute=torch.float16 if compute is None else compute, sel_out=x["sel"], workspace=ws, status=status,
+            events=events,
             carry=(x["sel"], MU) if x.get("carried") else None, defer=True)
     x["carried"] = True
 
@@ -327,7 +327,11 @@ def run_ours(args):
     dev_status = int(status.item())
     # the same step with rows ranked by their L2 norm (exact sums of squares), as the
     # benchmark configuration words it; same state chain, same number of steps
-    step_l2 = time_l2_steps(torch, d3, mbs, ws, status, args, K)
+    step_l2 = time_variant_steps(torch, d3, mbs, ws, status, K, "the headline step with norm_p=2 (rows ranked by "
+                                 "exact sums of squares, i.e. by row L2 norm), same megabatches and state chain",
+                                 norm_p=2)
+    step_bf16 = time_variant_steps(torch, d3, mbs, ws, status, K, "the headline step with bfloat16 Gram iterates "
+                                   "(fp32 accumulation), same megabatches and state chain", compute=torch.bfloat16)
 
     # phase split (sum over steps, per megabatch)
     names = ["momentum_keys", "select", "gather", "gram_ns_products"]
@@ -408,6 +412,7 @@ def run_ours(args):
         "roofline": roof,
         "phases": phases,
         "step_l2_selection": step_l2,
+        "step_bf16_iterates": step_bf16,
         "gpu_launches": K * len(mbs) * launches_per_mb,
         "clocks": clk,
         "device_status": dev_status,
