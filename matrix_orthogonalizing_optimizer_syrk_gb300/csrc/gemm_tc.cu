@@ -275,12 +275,15 @@ __device__ __forceinline__ void epi_dispatch(const KParams& p, int b, int r, int
 using dev::pack2;
 using dev::unpack2;
 
-// True when either 16-bit value of the pair is an infinity or a NaN (all exponent bits set).
+// Non-finite test of 16-bit pairs by carries: (w & E) + A sets bit 15 (31) of a half-word exactly
+// when its exponent bits are all ones (an infinity or a NaN), and never carries into the other
+// half.  OR-ing the sums of many pairs and testing 0x80008000 once checks them all.
 template <typename T>
-__device__ __forceinline__ bool nonfinite_pair(uint32_t w) {
-  constexpr uint32_t E = std::is_same<T, __half>::value ? 0x7C00u : 0x7F80u;
-  return (w & E) == E || ((w >> 16) & E) == E;
-}
+struct NonFinite16 {
+  static constexpr uint32_t E = std::is_same<T, __half>::value ? 0x7C007C00u : 0x7F807F80u;
+  static constexpr uint32_t A = std::is_same<T, __half>::value ? 0x04000400u : 0x00800080u;
+  static __device__ __forceinline__ uint32_t acc(uint32_t w, uint32_t keep) { return ((w & keep) & E) + (A & keep); }
+};
 
 // One lane of each warp that saw a non-finite value sets DION3_DEV_NONFINITE (warp-uniform call).
 __device__ __forceinline__ void flag_nonfinite(const KParams& p, bool bad, int lane) {
@@ -396,9 +399,18 @@ __device__ __forceinline__ void epi_tile_tma(const KParams& p, const CUtensorMap
       w[i] = pack2<T>(lo, hi);
     }
     if (p.check_finite && r < p.M) {
+      uint32_t carry = 0u;
+      if (c0 + 32 <= p.N) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        if (c0 + 2 * i < p.N) bad |= nonfinite_pair<T>(c0 + 2 * i + 1 < p.N ? w[i] : (w[i] & 0xFFFFu));
+        for (int i = 0; i < 16; ++i) carry |= NonFinite16<T>::acc(w[i], 0xFFFFFFFFu);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t keep = c0 + 2 * i < p.N ? (c0 + 2 * i + 1 < p.N ? 0xFFFFFFFFu : 0x0000FFFFu) : 0u;
+          carry |= NonFinite16<T>::acc(w[i], keep);
+        }
+      }
+      bad |= (carry & 0x80008000u) != 0u;
     }
     const bool diag = (EPI == EPI_SYM) && (c0 == r0w);
     const bool below = (EPI == EPI_SYM) && (c0 < r0w);
@@ -558,12 +570,15 @@ __device__ __forceinline__ void epi_tile_wupd(const KParams& p, uint8_t* stg, ui
         y.z = fmaf(a.z, ab, y.z);
         y.w = fmaf(a.w, ab, y.w);
         float* w = wr[it];
-        if (w != nullptr)
-          bad |= (c < p.N && !isfinite(y.x)) || (c + 1 < p.N && !isfinite(y.y)) || (c + 2 < p.N && !isfinite(y.z)) ||
-                 (c + 3 < p.N && !isfinite(y.w));
         if (full_chunk) {
+          // one sum per four values; only a non-finite sum (a non-finite value, or a sum of
+          // huge ones) is looked at value by value
+          if (!isfinite((y.x + y.y) + (y.z + y.w)))
+            bad |= !(isfinite(y.x) && isfinite(y.y) && isfinite(y.z) && isfinite(y.w));
           *reinterpret_cast<float4*>(w + c) = y;
         } else if (w != nullptr) {
+          bad |= (c < p.N && !isfinite(y.x)) || (c + 1 < p.N && !isfinite(y.y)) || (c + 2 < p.N && !isfinite(y.z)) ||
+                 (c + 3 < p.N && !isfinite(y.w));
           if (c < p.N) w[c] = y.x;
           if (c + 1 < p.N) w[c + 1] = y.y;
           if (c + 2 < p.N) w[c + 2] = y.z;

@@ -37,7 +37,7 @@ out = {{}}
 status = torch.zeros(1, dtype=torch.int32, device=dev)
 # symmetric GEMM (pair tiles and a ragged single-tile product), Gram NS (separate products and
 # fused segments), standard NS
-A = synthetic.gaussian((2, 700, 300), seed=1, std=300 ** -0.5, dtype=torch.bfloat16, device=dev)
+A = synthetic.gaussian((2, 700, 320), seed=1, std=320 ** -0.5, dtype=torch.bfloat16, device=dev)
 out["sym"] = d3.sym_gemm(A, status=status).float()
 X = synthetic.lowrank_batch(3, 200, 640, base_seed=2, dtype=torch.bfloat16, device=dev)
 out["gram"] = d3.gram_ns(X, ABC, (2, 4), status=status).float()
