@@ -60,3 +60,28 @@ def test_carried_step_passes_the_previous_selection():
     assert calls[0]["carry"] is None
     assert all(c["carry"] == ("sel", bench.MU) for c in calls[1:])
     assert all(c["defer"] is True and c["sel_out"] == "sel" for c in calls)
+
+
+def test_roofline_peak_follows_the_clock_record():
+    """The burst bf16 figure was measured at the maximum SM clock: it is the denominator when the
+    run's median clock sat within 3% of the maximum; otherwise (or without a clock record) the
+    sustained one is."""
+    assert bench.clock_at_max({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0})
+    assert bench.clock_at_max({"sm_mhz": 2010.0, "sm_max_mhz": 2070.0})
+    assert not bench.clock_at_max({"sm_mhz": 1995.0, "sm_max_mhz": 2070.0})
+    assert not bench.clock_at_max({"sm_mhz": 1515.0, "sm_max_mhz": 2070.0})
+    assert not bench.clock_at_max({"error": "nvidia-smi unavailable"})
+    assert not bench.clock_at_max(None)
+
+
+@pytest.mark.parametrize("B,expect", [(128, [0, 64, 127]), (96, [0, 48, 95]), (2, [0, 1]), (1, [0])])
+def test_oracle_sample_is_first_middle_last(B, expect):
+    assert bench.sample_indices(B) == expect
+
+
+def test_recorded_traffic_is_keyed_to_the_kernel_source():
+    """traffic.json holds a per-launch byte count for the GEMM family, valid only for the source it
+    was measured on: the bench reports it when the hash matches, null for an unknown kernel."""
+    v = bench.recorded_traffic("tc_gemm_kernel (all tcgen05 GEMM launches of the Gram-NS chain)")
+    assert v is None or 1e9 < v < 3e9
+    assert bench.recorded_traffic("no such kernel") is None
