@@ -605,7 +605,7 @@ def bench_moe_step(torch, d3, synthetic, dev, peaks, peaks_kind):
 
     def fn(events=None):
         d3.step(W, M, Gs[state["s"] % 2], f=fk, mu=MU, eta=ETA, norm_p=1, abc=ABC, restart_after=RESTARTS,
-                compute=torch.float16, sel_out=sel, workspace=ws, events=events,
+                compute=state.get("compute", torch.float16), sel_out=sel, workspace=ws, events=events,
                 carry=(sel, MU) if state["s"] > 0 else None, defer=True)
         state["s"] += 1
 
@@ -616,12 +616,19 @@ def bench_moe_step(torch, d3, synthetic, dev, peaks, peaks_kind):
     fn(evs)
     torch.cuda.synchronize()
     ph = [evs[i].elapsed_time(evs[i + 1]) for i in range(4)]
+    # the same carried step with bfloat16 Gram iterates (the configuration's precision word)
+    state["compute"] = torch.bfloat16
+    for _ in range(2):
+        fn()
+    torch.cuda.synchronize()
+    ms_bf16 = _time_calls(torch, fn, 5)
     hbm = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
     bytes_a = 10.0 * B * n * m
     bytes_c = GATHER_BYTES * B * k * m
     out = {"workload": "dion3_step f=1/8 on 3072 x 768x2048 (MoE experts), T=5 Jordan, restarts 2,4, fp16 iterates, "
                        "decay of M[S] carried",
-           "ms": ms, "phases_ms": {"momentum_keys": ph[0], "select": ph[1], "gather": ph[2], "gram_ns_products": ph[3]},
+           "ms": ms, "ms_bf16_iterates": ms_bf16,
+           "phases_ms": {"momentum_keys": ph[0], "select": ph[1], "gather": ph[2], "gram_ns_products": ph[3]},
            "momentum_frac_hbm": bytes_a / ph[0] / 1e6 / hbm,
            "hbm_floor_ms": (bytes_a + bytes_c) / hbm / 1e6,
            "peak_source": f"{peaks_kind} hbm_gbs"}

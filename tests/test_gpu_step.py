@@ -132,14 +132,14 @@ def test_nonfinite_gradient_sets_status():
 
 
 @pytest.mark.parametrize("shape,count,f,norm_p,computes", [
-    ((768, 2048), 3072, (1, 8), 1, (torch.float16,)),
+    ((768, 2048), 3072, (1, 8), 1, (torch.float16, torch.bfloat16)),
     ((4096, 4096), 128, (1, 4), 1, (torch.float16, torch.bfloat16)),
     ((4096, 11008), 96, (1, 4), 1, (torch.float16, torch.bfloat16)),
     ((4096, 11008), 96, (1, 4), 2, (torch.float16,)),
 ])
 def test_megabatch_full_size_two_steps(shape, count, f, norm_p, computes):
-    """Full-size megabatches (MoE experts at f = 1/8; 7B dense shapes at f = 1/4 with float16 and
-    bfloat16 Gram iterates; the 4096 x 11008 batch also with row L2 selection, where the exact
+    """Full-size megabatches (MoE experts at f = 1/8 and 7B dense shapes at f = 1/4, each with float16
+    and bfloat16 Gram iterates; the 4096 x 11008 batch also with row L2 selection, where the exact
     re-rank sums 11008 squares per row): matrices 0, B/2 and B-1 against the oracle over two
     steps (the second starts from error-feedback state).  Rows and M bit-exact, Delta W <= 3e-2.
 
