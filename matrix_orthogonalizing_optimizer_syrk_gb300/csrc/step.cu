@@ -234,20 +234,57 @@ __device__ uint32_t radix_kth_largest(const uint32_t* v, int n, int k, uint32_t*
   return prefix;
 }
 
-template <int NL>
-__device__ void limbs_add_shifted(uint64_t (&L)[NL], uint64_t v, int sh) {
-  if (v == 0) return;
-  const int li = sh >> 6, off = sh & 63;
-  const uint64_t lo = v << off;
-  const uint64_t hi = off ? (v >> (64 - off)) : 0ull;
-  uint64_t old = L[li];
-  L[li] += lo;
-  uint64_t add = hi + (L[li] < old ? 1ull : 0ull);
-  for (int q = li + 1; add != 0 && q < NL; ++q) {
-    old = L[q];
-    L[q] += add;
-    add = L[q] < old ? 1ull : 0ull;
+// Adds v << off (v < 2^40, off < 64) into the 128-bit value (hi, lo).
+__device__ __forceinline__ void add_shifted128(uint64_t& lo, uint64_t& hi, uint64_t v, int off) {
+  const uint64_t l = v << off;
+  lo += l;
+  hi += (off ? v >> (64 - off) : 0ull) + (lo < l ? 1ull : 0ull);
+}
+
+// The exact key of one row from its exponent buckets, written as NL little-endian 64-bit limbs
+// to `out` (value * 2^149 for norm_p = 1: sum over w of bkt[w] 2^w; value * 2^298 for norm_p = 2:
+// sum of bkt[w] 2^(2w) and bkt[256 + w] 2^(2w + 24)).  Warp 0 only: lane q < NL adds the
+// buckets whose shift falls in [64q, 64q + 64) into 128 bits (at most 64 terms below 2^103), then
+// lane 0 chains the carries.  `part` holds 2 NL words of shared memory.
+template <int NORM_P, int NL>
+__device__ void buckets_to_limbs(const unsigned long long* bkt, uint64_t* part, uint64_t* out) {
+  const int q = threadIdx.x;
+  if (q < NL) {
+    uint64_t lo = 0ull, hi = 0ull;
+    const int s0 = 64 * q;
+    if constexpr (NORM_P == 1) {
+      for (int w = s0; w < s0 + 64 && w < 256; ++w) add_shifted128(lo, hi, bkt[w], w - s0);
+    } else {
+      for (int w = s0 / 2; w < s0 / 2 + 32 && w < 256; ++w) add_shifted128(lo, hi, bkt[w], 2 * w - s0);
+      for (int w = max(0, s0 / 2 - 12); w < s0 / 2 + 20 && w < 256; ++w)
+        add_shifted128(lo, hi, bkt[256 + w], 2 * w + 24 - s0);
+    }
+    part[2 * q] = lo;
+    part[2 * q + 1] = hi;
   }
+  __syncwarp();
+  if (q == 0) {
+    uint64_t carry = 0ull;  // the previous window's high word plus the carry out of its limb
+    for (int l = 0; l < NL; ++l) {
+      const uint64_t lo = part[2 * l];
+      const uint64_t v = lo + carry;
+      out[l] = v;
+      carry = part[2 * l + 1] + (v < lo ? 1ull : 0ull);
+    }
+  }
+}
+
+// Digit p (most significant first, 8 bits each) of the unique sort key (exact key, 0xFFFF - row)
+// of ambiguous entry j: the NL limbs of the key, then two digits of the inverted row index, so
+// that equal keys rank the lower row first.
+template <int NL>
+__device__ __forceinline__ uint32_t rank_digit(const uint64_t* ex, int j, int row, int p) {
+  if (p < NL * 8) {
+    const uint64_t limb = ex[static_cast<long long>(j) * NL + (NL - 1 - p / 8)];
+    return static_cast<uint32_t>(limb >> (56 - 8 * (p % 8))) & 255u;
+  }
+  const uint32_t inv = 0xFFFFu - static_cast<uint32_t>(row);
+  return p == NL * 8 ? (inv >> 8) & 255u : inv & 255u;
 }
 
 template <int NL>
@@ -303,6 +340,7 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const BArgs a) {
   __shared__ int warp_sums[32];
   __shared__ int sh[4];
   __shared__ int s_bad;
+  __shared__ uint64_t s_part[2 * NL];
 
   const int b = blockIdx.x, n = a.n, k = a.k, tid = threadIdx.x, bd = blockDim.x;
   int32_t* sel = a.sel + static_cast<long long>(b) * k;
@@ -358,67 +396,106 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const BArgs a) {
       __syncthreads();
       const uint32_t* src =
           reinterpret_cast<const uint32_t*>(a.M + static_cast<long long>(b) * n * a.m + row * a.kstride);
-      for (int base = 0; base < a.m; base += bd) {
-        const int e = base + tid;
-        const uint32_t bits = e < a.m ? src[e * a.estride] : 0u;
-        const uint32_t e8 = (bits >> 23) & 255u;
-        uint32_t mant = (bits & 0x7FFFFFu) | (e8 ? 0x800000u : 0u);
-        if (e8 == 255u) {
-          s_bad = 1;
-          mant = 0;
+      // Four loads in flight per thread; lanes past the row's end contribute zero.
+      for (int base = 0; base < a.m; base += 4 * bd) {
+        uint32_t bits4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = base + u * bd + tid;
+          bits4[u] = e < a.m ? src[e * a.estride] : 0u;
         }
-        const uint32_t w = e8 ? e8 - 1u : 0u;
-        const unsigned grp = __match_any_sync(0xffffffffu, w);
-        const bool leader = (threadIdx.x & 31) == (__ffs(grp) - 1);
-        if constexpr (NORM_P == 1) {
-          const unsigned sum = __reduce_add_sync(grp, mant);
-          if (leader && sum) atomicAdd(&bkt[w], static_cast<unsigned long long>(sum));
-        } else {
-          const uint64_t sq = static_cast<uint64_t>(mant) * mant;
-          const unsigned l24 = static_cast<unsigned>(sq & 0xFFFFFFull);
-          const unsigned h24 = static_cast<unsigned>(sq >> 24);
-          const unsigned sl = __reduce_add_sync(grp, l24);
-          const unsigned shh = __reduce_add_sync(grp, h24);
-          if (leader) {
-            if (sl) atomicAdd(&bkt[w], static_cast<unsigned long long>(sl));
-            if (shh) atomicAdd(&bkt[256 + w], static_cast<unsigned long long>(shh));
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t bits = bits4[u];
+          const uint32_t e8 = (bits >> 23) & 255u;
+          uint32_t mant = (bits & 0x7FFFFFu) | (e8 ? 0x800000u : 0u);
+          if (e8 == 255u) {
+            s_bad = 1;
+            mant = 0;
           }
-        }
-      }
-      __syncthreads();
-      if (tid == 0) {
-        uint64_t Lm[NL];
-#pragma unroll
-        for (int q = 0; q < NL; ++q) Lm[q] = 0ull;
-        if (s_bad) {
-#pragma unroll
-          for (int q = 0; q < NL; ++q) Lm[q] = ~0ull;
-          if (a.status) atomicOr(a.status, DION3_DEV_NONFINITE);
-        } else {
-          for (int w = 0; w < 256; ++w) {
-            if constexpr (NORM_P == 1) {
-              limbs_add_shifted<NL>(Lm, bkt[w], w);  // value * 2^149 = sum mant * 2^w
-            } else {
-              limbs_add_shifted<NL>(Lm, bkt[w], 2 * w);             // value * 2^298
-              limbs_add_shifted<NL>(Lm, bkt[256 + w], 2 * w + 24);
+          const uint32_t w = e8 ? e8 - 1u : 0u;
+          const unsigned grp = __match_any_sync(0xffffffffu, w);
+          const bool leader = (threadIdx.x & 31) == (__ffs(grp) - 1);
+          if constexpr (NORM_P == 1) {
+            const unsigned sum = __reduce_add_sync(grp, mant);
+            if (leader && sum) atomicAdd(&bkt[w], static_cast<unsigned long long>(sum));
+          } else {
+            const uint64_t sq = static_cast<uint64_t>(mant) * mant;
+            const unsigned l24 = static_cast<unsigned>(sq & 0xFFFFFFull);
+            const unsigned h24 = static_cast<unsigned>(sq >> 24);
+            const unsigned sl = __reduce_add_sync(grp, l24);
+            const unsigned shh = __reduce_add_sync(grp, h24);
+            if (leader) {
+              if (sl) atomicAdd(&bkt[w], static_cast<unsigned long long>(sl));
+              if (shh) atomicAdd(&bkt[256 + w], static_cast<unsigned long long>(shh));
             }
           }
         }
-        for (int q = 0; q < NL; ++q) ex[static_cast<long long>(j) * NL + q] = Lm[q];
-        s_bad = 0;
       }
       __syncthreads();
-    }
-    for (int j = tid; j < tot_amb; j += bd) {
-      const uint64_t* kj = ex + static_cast<long long>(j) * NL;
-      const int ij = amb[j];
-      int rank = 0;
-      for (int q = 0; q < tot_amb; ++q) {
-        if (q == j) continue;
-        const int cmp = limbs_cmp<NL>(ex + static_cast<long long>(q) * NL, kj);
-        if (cmp > 0 || (cmp == 0 && amb[q] < ij)) ++rank;
+      uint64_t* exj = ex + static_cast<long long>(j) * NL;
+      if (s_bad) {
+        if (tid < NL) exj[tid] = ~0ull;
+        if (tid == 0 && a.status) atomicOr(a.status, DION3_DEV_NONFINITE);
+      } else if (tid < 32) {
+        buckets_to_limbs<NORM_P, NL>(bkt, s_part, exj);
       }
-      flag[ij] = rank < r ? 1 : 0;
+      __syncthreads();
+      if (tid == 0) s_bad = 0;  // every thread has read it; the next row's barrier follows
+    }
+    if (tot_amb <= bd) {
+      // Few ambiguous rows: each thread ranks one against all others.
+      for (int j = tid; j < tot_amb; j += bd) {
+        const uint64_t* kj = ex + static_cast<long long>(j) * NL;
+        const int ij = amb[j];
+        int rank = 0;
+        for (int q = 0; q < tot_amb; ++q) {
+          if (q == j) continue;
+          const int cmp = limbs_cmp<NL>(ex + static_cast<long long>(q) * NL, kj);
+          if (cmp > 0 || (cmp == 0 && amb[q] < ij)) ++rank;
+        }
+        flag[ij] = rank < r ? 1 : 0;
+      }
+    } else {
+      // Many (ties, e.g. rows that are permutations of one another): MSB-first radix select of
+      // the r largest unique sort keys (exact key, 0xFFFF - row).  Candidates keep flag 2; each
+      // digit marks those above the r-th candidate's digit in (1) and those below out (0).
+      // Invariant: at least rr candidates remain, and rr of them are still to be taken.
+      int rr = r;
+      for (int p = 0; p < NL * 8 + 2; ++p) {
+        for (int q = tid; q < 256; q += bd) hist[q] = 0;
+        __syncthreads();
+        for (int j = tid; j < tot_amb; j += bd) {
+          const int row = amb[j];
+          if (flag[row] == 2) atomicAdd(&hist[rank_digit<NL>(ex, j, row, p)], 1u);
+        }
+        __syncthreads();
+        if (tid == 0) {
+          int cum = 0, d = 255;
+          for (; d > 0; --d) {
+            if (cum + static_cast<int>(hist[d]) >= rr) break;
+            cum += static_cast<int>(hist[d]);
+          }
+          sh[0] = d;
+          sh[1] = rr - cum;
+          sh[2] = static_cast<int>(hist[d]);
+        }
+        __syncthreads();
+        const uint32_t d = static_cast<uint32_t>(sh[0]);
+        for (int j = tid; j < tot_amb; j += bd) {
+          const int row = amb[j];
+          if (flag[row] != 2) continue;
+          const uint32_t dj = rank_digit<NL>(ex, j, row, p);
+          if (dj != d) flag[row] = dj > d ? 1 : 0;
+        }
+        rr = sh[1];
+        const bool done = sh[2] == rr;  // every remaining candidate is taken
+        __syncthreads();
+        if (done) break;
+      }
+      // The keys are unique, so the loop ends with exactly rr candidates left, all taken.
+      for (int j = tid; j < tot_amb; j += bd)
+        if (flag[amb[j]] == 2) flag[amb[j]] = 1;
     }
   } else {
     for (int j = tid; j < tot_amb; j += bd) flag[amb[j]] = (r == tot_amb) ? 1 : 0;

@@ -253,3 +253,150 @@ def test_invalid_given_rows_leave_that_matrix_unselected():
                                      rows=rows[0])
     assert np.array_equal(bits32(M[0]), bits32(M1))
     assert rel_frob(W[0].double().cpu().numpy() - W0[0], W1 - W0[0]) <= 3e-2
+
+
+
+
+def _permuted_rows(n: int, m: int, seed: int):
+    """fp32 M and bf16 G, [n, m], whose row i is the same column permutation p_i of one fp32 and
+    one bf16 vector, so that every row of M + G is a permutation of one row."""
+    rng = np.random.default_rng(seed)
+    perm = torch.from_numpy(np.stack([rng.permutation(m) for _ in range(n)])).to(DEV)
+    vm = synthetic.gaussian((m,), seed=seed + 1, std=0.05, device=DEV)
+    vg = synthetic.gaussian((m,), seed=seed + 2, std=0.01, dtype=torch.bfloat16, device=DEV)
+    return vm[perm], vg[perm]
+
+
+@pytest.mark.parametrize("norm_p", [1, 2])
+def test_tied_rows_more_ambiguous_than_threads(norm_p):
+    """Selection when most rows tie exactly, so that more rows straddle the boundary than the
+    selection block has threads and the exact ranking takes its radix-select route.  Matrix 0:
+    rows that are permutations of one row, 64 of them (G zero there) one ulp smaller or larger in
+    their largest entry.  Matrix 1: all zero, every key 0, S = {0, ..., k-1} and no update.
+    Full oracle parity: rows bit-exact, M bit-exact, Delta W within 3e-2."""
+    n = m = 2048
+    M = torch.zeros((2, n, m), dtype=torch.float32, device=DEV)
+    G = torch.zeros((2, n, m), dtype=torch.bfloat16, device=DEV)
+    M[0], G[0] = _permuted_rows(n, m, 81)
+    rng = np.random.default_rng(84)
+    rows = np.sort(rng.choice(n, 64, replace=False))
+    ri = torch.from_numpy(rows).to(DEV)
+    P = (M[0, ri].cpu().numpy().astype(np.float64) + G[0, ri].float().cpu().numpy()).astype(np.float32)
+    P.view(np.int32)[np.arange(64), np.argmax(np.abs(P), axis=1)] += np.where(rng.random(64) < 0.5, -1, 1).astype(np.int32)
+    M[0, ri] = torch.from_numpy(P).to(DEV)
+    G[0, ri] = 0
+    W = synthetic.gaussian((2, n, m), seed=85, std=0.02, device=DEV)
+    W1_zero = W[1].clone()
+    sel = _run_and_check(W, M, G, (1, 4), 0.95, 0.01, norm_p, (2, 4))
+    k = d3.k_of(n, 1, 4)
+    assert np.array_equal(sel[1].cpu().numpy(), np.arange(k))
+    assert torch.equal(W[1], W1_zero)
+
+
+def _approx_keys(M1: np.ndarray, norm_p: int) -> np.ndarray:
+    """float64 sums of |x| (or x^2) per row: every term is exact in float64 and numpy's pairwise
+    sum of at most 65536 nonnegative terms is within 1e-14 relative of the exact key."""
+    x = np.abs(M1.astype(np.float64))
+    return x.sum(axis=1) if norm_p == 1 else (x * x).sum(axis=1)
+
+
+def _expected_rows(M1: np.ndarray, k: int, norm_p: int) -> np.ndarray:
+    """The k rows of largest exact key, ties to the lower index, ascending -- without exact keys
+    for every row: the float64 sums settle each row more than 1e-9 relative away from the k-th
+    sum, and the oracle's exact integer keys rank the rows inside that margin."""
+    approx = _approx_keys(M1, norm_p)
+    kth = np.sort(approx)[::-1][k - 1]
+    sure = np.where(approx > kth * (1 + 1e-9))[0]
+    amb = np.where(np.abs(approx - kth) <= kth * 1e-9)[0]
+    assert len(sure) <= k <= len(sure) + len(amb)
+    exact = oracle.exact_row_keys(np.ascontiguousarray(M1[amb]), norm_p)
+    ranked = sorted(range(len(amb)), key=lambda i: (-exact[i], amb[i]))
+    return np.sort(np.concatenate([sure, amb[ranked[:k - len(sure)]]]))
+
+
+@pytest.mark.parametrize("n,m,f", [(16384, 16384, (1, 4)), (1024, 65536, (1, 8))])
+@pytest.mark.parametrize("norm_p", [1, 2])
+def test_boundary_ties_at_the_maximum_sizes(n, m, f, norm_p):
+    """The step's size limits (n = 16384 rows, m = 65536 columns) with the k-th largest key inside
+    a group of tied rows: the 64 rows of smallest key are rewritten (G = 0 there) as column
+    permutations of the row ranked k - 32 -- equal exact keys, unequal fp32 sums -- and then the
+    lowest-indexed of them loses one ulp in its largest entry and the highest-indexed gains one.
+    The fp32 key intervals cannot order the group, so the exact integer re-rank runs on rows of
+    full width.  Rows bit-exact against exact keys, M bit-exact, W changed on exactly the selected
+    rows, and (where the oracle's float64 Gram Newton-Schulz of the k selected rows is quick)
+    Delta W within 3e-2 of the oracle's.  Gradients are Gaussian here: the selection sees only M + G."""
+    k = d3.k_of(n, *f)
+    g = 64
+    rng = np.random.default_rng(1000 * norm_p + m // n)
+    M = synthetic.gaussian((1, n, m), seed=71, std=0.05, device=DEV)
+    G = synthetic.gaussian((1, n, m), seed=72, std=0.01, dtype=torch.bfloat16, device=DEV)
+    W = synthetic.gaussian((1, n, m), seed=73, std=0.02, device=DEV)
+    M1 = (M[0].cpu().numpy().astype(np.float64) + G[0].float().cpu().numpy()).astype(np.float32)
+    order = np.argsort(-_approx_keys(M1, norm_p), kind="stable")
+    base = int(order[k - g // 2 - 1])
+    group = np.sort(order[-g:])
+    row = M1[base].copy()
+    for r in group:
+        M1[r] = row[rng.permutation(m)]
+    bits = M1.view(np.int32)
+    bits[group[0], int(np.argmax(np.abs(M1[group[0]])))] -= 1   # |x| one ulp smaller
+    bits[group[-1], int(np.argmax(np.abs(M1[group[-1]])))] += 1  # |x| one ulp larger
+    gi = torch.from_numpy(group).to(DEV)
+    M[0, gi] = torch.from_numpy(M1[group]).to(DEV)
+    G[0, gi] = 0
+    W0 = W[0].cpu().numpy().copy()
+    S = _expected_rows(M1, k, norm_p)
+    assert group[-1] in S and group[0] not in S
+
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sel = d3.step(W, M, G, f=f, mu=0.95, eta=0.01, norm_p=norm_p, abc=ABC, restart_after=(2, 4), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(sel[0].cpu().numpy().astype(np.int64), S)
+    Mexp = M1.copy()
+    Mexp[S] = (np.float64(np.float32(0.95)) * M1[S].astype(np.float64)).astype(np.float32)
+    assert np.array_equal(bits32(M[0]), Mexp.view(np.uint32))
+    W1 = W[0].cpu().numpy()
+    keep = np.ones(n, dtype=bool)
+    keep[S] = False
+    assert np.array_equal(W1[keep].view(np.uint32), W0[keep].view(np.uint32))
+    assert np.isfinite(W1[S]).all()
+    if k * k * m <= 2**30:
+        O = oracle.gram_ns(M1[S].astype(np.float64), ABC, (2, 4))
+        eta_p = 0.01 * np.sqrt(f[1] / f[0])
+        assert rel_frob(W1[S].astype(np.float64) - W0[S], -eta_p * O) <= 3e-2
+
+
+@pytest.mark.parametrize("norm_p", [1, 2])
+def test_all_rows_tied_at_the_maximum_n(norm_p):
+    """n = m = 16384 with every row of M and of G the same column permutation of one row, so
+    every row of M + G is a permutation of one row: equal exact keys, fp32 sums that differ with
+    the order.  Every row straddles the boundary, the exact re-rank runs on all 16384 rows, and
+    ties to the lower index make S = {0, ..., k-1}.  M bit-exact, W changed on rows < k only."""
+    n = m = 16384
+    k = d3.k_of(n, 1, 4)
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(76 + norm_p)
+    perm = torch.argsort(torch.rand((n, m), generator=gen, device=DEV), dim=1)
+    vm = synthetic.gaussian((m,), seed=74, std=0.05, device=DEV)
+    vg = synthetic.gaussian((m,), seed=75, std=0.01, dtype=torch.bfloat16, device=DEV)
+    M = vm[perm].unsqueeze(0).contiguous()
+    G = vg[perm].unsqueeze(0).contiguous()
+    W = synthetic.gaussian((1, n, m), seed=77, std=0.02, device=DEV)
+    W0 = W[0].cpu().numpy().copy()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sel = d3.step(W, M, G, f=(1, 4), mu=0.95, eta=0.01, norm_p=norm_p, abc=ABC, restart_after=(2, 4),
+                  status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(sel[0].cpu().numpy(), np.arange(k))
+    v1 = (vm.double().cpu().numpy() + vg.double().cpu().numpy()).astype(np.float32)
+    v2 = (np.float64(np.float32(0.95)) * v1.astype(np.float64)).astype(np.float32)
+    p = perm.cpu().numpy()
+    del perm
+    Mh = bits32(M[0])
+    assert np.array_equal(Mh[:k], v2.view(np.uint32)[p[:k]])
+    assert np.array_equal(Mh[k:], v1.view(np.uint32)[p[k:]])
+    W1 = W[0].cpu().numpy()
+    assert np.array_equal(W1[k:].view(np.uint32), W0[k:].view(np.uint32))
+    assert np.isfinite(W1[:k]).all() and not np.array_equal(W1[:k], W0[:k])

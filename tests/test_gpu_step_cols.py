@@ -97,3 +97,20 @@ def test_column_ties_and_near_ties():
     for norm_p in (1, 2):
         _check(torch.zeros((1, m, 40), device=DEV), torch.zeros((1, m, 40), device=DEV), G2, (1, 4), norm_p=norm_p,
                check_w=False)
+
+
+@pytest.mark.parametrize("norm_p", [1, 2])
+def test_tied_columns(norm_p):
+    """Every column of M + G the same permutation of one column (equal exact keys, fp32 sums that
+    differ with the order): more ambiguous columns than the selection block has threads, so the
+    radix-select ranking reads the strided column vectors; ties take the lower column index."""
+    m, n = 2048, 512
+    rng = np.random.default_rng(91)
+    perm = torch.from_numpy(np.stack([rng.permutation(m) for _ in range(n)])).to(DEV)
+    vm = synthetic.gaussian((m,), seed=92, std=0.05, device=DEV)
+    vg = synthetic.gaussian((m,), seed=93, std=0.01, dtype=torch.bfloat16, device=DEV)
+    M = vm[perm].T.contiguous().unsqueeze(0)
+    G = vg[perm].T.contiguous().unsqueeze(0)
+    W = synthetic.gaussian((1, m, n), seed=94, std=0.02, device=DEV)
+    sel = _check(W, M, G, (1, 4), norm_p=norm_p)
+    assert np.array_equal(sel[0].cpu().numpy(), np.arange(d3.k_of(n, 1, 4)))
