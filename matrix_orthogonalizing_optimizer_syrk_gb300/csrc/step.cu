@@ -330,8 +330,10 @@ __device__ void selected_scale(const BArgs& a, int b, const int32_t* sel) {
 }
 
 // ------------------------------------------------------------------------------ pass B
-template <int NORM_P>
-__global__ void __launch_bounds__(SEL_THREADS) select_kernel(const BArgs a) {
+// THREADS = 256 (n <= 2048: many small matrices, e.g. MoE experts) is bounded to 32 registers so
+// that eight CTAs share an SM; THREADS = 1024 runs one large matrix per CTA.
+template <int NORM_P, int THREADS>
+__global__ void __launch_bounds__(THREADS, THREADS == 256 ? 8 : 1) select_kernel(const BArgs a) {
   constexpr int NL = NORM_P == 1 ? 5 : 9;
   constexpr int NB = NORM_P == 1 ? 256 : 512;
   extern __shared__ __align__(16) uint8_t sm[];
@@ -753,16 +755,18 @@ int step_select(const StepArgs& s, cudaStream_t st) {
   const int smem = 11 * s.n + 16;
   // One CTA per matrix; small matrices (many of them, e.g. MoE experts) get 256 threads so that
   // several CTAs share an SM.
-  const int threads = s.n <= 2048 ? 256 : SEL_THREADS;
-  if (s.norm_p == 1) {
-    if (cudaFuncSetAttribute(select_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return DION3_ECUDA;
-    select_kernel<1><<<s.batch, threads, smem, st>>>(a);
-  } else {
-    if (cudaFuncSetAttribute(select_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return DION3_ECUDA;
-    select_kernel<2><<<s.batch, threads, smem, st>>>(a);
-  }
+  auto launch = [&](auto kern, int threads) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return false;
+    kern<<<s.batch, threads, smem, st>>>(a);
+    return true;
+  };
+  bool ok;
+  if (s.n <= 2048)
+    ok = s.norm_p == 1 ? launch(select_kernel<1, 256>, 256) : launch(select_kernel<2, 256>, 256);
+  else
+    ok = s.norm_p == 1 ? launch(select_kernel<1, SEL_THREADS>, SEL_THREADS)
+                       : launch(select_kernel<2, SEL_THREADS>, SEL_THREADS);
+  if (!ok) return DION3_ECUDA;
   return cudaGetLastError() == cudaSuccess ? DION3_OK : DION3_ECUDA;
 }
 

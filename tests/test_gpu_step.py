@@ -102,6 +102,33 @@ def test_near_ties_resolved_exactly():
             _run_and_check(W.clone(), M.clone(), G, f, 0.95, 0.01, norm_p, (2,), check_w=False)
 
 
+
+@pytest.mark.parametrize("n,m,f", [(1, 1, (1, 1)), (1, 8, (1, 4)), (2, 3, (1, 2)), (3, 17, (1, 8)), (8, 8, (1, 1)),
+                                   (17, 40, (1, 4))])
+@pytest.mark.parametrize("norm_p", [1, 2])
+def test_tiny_shapes(n, m, f, norm_p):
+    """Degenerate sizes: one row, k = 1 of 3 rows, square matrices, rows of 1 to 3 elements
+    (no vector path; rows inside the batch not 16-byte aligned).  Two chained steps on a batch
+    of three against the oracle."""
+    batch = 3
+    W = synthetic.gaussian((batch, n, m), seed=5, std=0.02, device=DEV)
+    M = torch.zeros((batch, n, m), dtype=torch.float32, device=DEV)
+    for step in range(2):
+        G = synthetic.lowrank_batch(batch, n, m, base_seed=700 + 100 * step + 10 * n + m, dtype=torch.bfloat16,
+                                    device=DEV)
+        _run_and_check(W, M, G, f, 0.95, 0.01, norm_p, (2, 4))
+
+
+def test_empty_batch_is_a_no_op():
+    """batch = 0: nothing to select or update; the call succeeds and returns no rows."""
+    W = torch.zeros((0, 64, 256), dtype=torch.float32, device=DEV)
+    M = torch.zeros_like(W)
+    G = torch.zeros((0, 64, 256), dtype=torch.bfloat16, device=DEV)
+    sel = d3.step(W, M, G, f=(1, 4), abc=ABC, restart_after=(2, 4))
+    torch.cuda.synchronize()
+    assert tuple(sel.shape) == (0, d3.k_of(64, 1, 4))
+
+
 @pytest.mark.parametrize("gdt", [torch.float32, torch.float16])
 def test_gradient_dtypes_and_weight_decay(gdt):
     n, m = 80, 320
