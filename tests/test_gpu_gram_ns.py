@@ -55,6 +55,23 @@ def test_bf16_input_fp16_iterates(n, m, restarts):
     assert rel_frob(to64(O), ref) <= 3e-2
 
 
+
+@pytest.mark.parametrize("n,m", [(1, 1), (2, 3), (3, 5), (5, 7), (7, 7)])
+@pytest.mark.parametrize("compute,tol", [(torch.float16, 3e-2), (torch.float32, 1e-4)])
+def test_rows_narrower_than_16_bytes(n, m, compute, tol):
+    """m < 8: X's rows are not 16-byte aligned (the call copies X into the workspace), every tile
+    is ragged; batched, with and without restarts."""
+    X = torch.stack([synthetic.lowrank_plus_noise(n, m, seed=40 + i, dtype=torch.bfloat16, device=DEV)
+                     for i in range(3)])
+    for restarts in ((), (2, 4)):
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        O = d3.gram_ns(X, ABC, restarts, compute=compute, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        for i in range(3):
+            assert rel_frob(to64(O[i]), oracle.gram_ns(to64(X[i]), ABC, restarts)) <= tol
+
+
 @pytest.mark.parametrize("n,m", SHAPES)
 def test_bf16_iterates_with_restarts(n, m):
     """All-bf16 iterates are coarser (8-bit mantissa); with restarts after 2 and 4 they stay in

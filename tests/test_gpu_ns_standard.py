@@ -46,6 +46,20 @@ def test_16bit_iterates(n, m, compute):
     assert int(status.item()) == 0
 
 
+
+@pytest.mark.parametrize("n,m", [(1, 1), (2, 3), (3, 3), (3, 5), (5, 7)])
+@pytest.mark.parametrize("compute,tol", [(torch.float16, 3e-2), (torch.float32, 1e-4)])
+def test_rows_narrower_than_16_bytes(n, m, compute, tol):
+    """m < 8: unaligned input rows and ragged tiles everywhere; a batch of three."""
+    X = torch.stack([synthetic.lowrank_plus_noise(n, m, seed=60 + i, dtype=torch.bfloat16, device=DEV)
+                     for i in range(3)])
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    O = d3.ns_standard(X, ABC, compute=compute, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert rel_frob(to64(O), _oracle(X)) <= tol
+
+
 @pytest.mark.parametrize("n,m", [(64, 64), (256, 256), (100, 333), (256, 1024)])
 def test_fp32_mode(n, m):
     X = synthetic.gaussian((n, m), seed=n * m, device=DEV)

@@ -57,6 +57,20 @@ def test_two_steps(m, n, f, norm_p):
         _check(W, M, G, f, norm_p=norm_p)
 
 
+
+@pytest.mark.parametrize("m,n,f", [(1, 1, (1, 1)), (3, 2, (1, 2)), (17, 3, (1, 8)), (40, 17, (1, 4))])
+@pytest.mark.parametrize("norm_p", [1, 2])
+def test_tiny_shapes(m, n, f, norm_p):
+    """Degenerate sizes for column selection: one column, k = 1, rows of 1 to 3 elements."""
+    batch = 3
+    W = synthetic.gaussian((batch, m, n), seed=52, std=0.02, device=DEV)
+    M = torch.zeros((batch, m, n), dtype=torch.float32, device=DEV)
+    for step in range(2):
+        G = synthetic.lowrank_batch(batch, m, n, base_seed=900 + 100 * step + 10 * m + n, dtype=torch.bfloat16,
+                                    device=DEV)
+        _check(W, M, G, f, norm_p=norm_p)
+
+
 def test_moe_w2_shape():
     """The MoE w2 matrices as stored (2048 x 768): columns are the short side; f = 1/8, k = 96."""
     batch = 2
